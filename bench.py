@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the online-softmax attention / softmax hot path on GB300.
+
+One JSON line on stdout (rank 0).  Default workload: the batched GQA causal prefill
+(B=2, Hq=32, Hkv=8, Sq=Sk=4096, D=128, bf16), whose bf16 tensor-core throughput is the headline
+attention metric; the other workloads (single-head fp32/bf16 4096x4096 d=64, the M=64 N=100
+d=32 single head, split-K decode, row softmax, 1-D softmax) are measured after it in the same
+run and reported under "suite".
+
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA events on the
+launching stream; L2 is flushed (a 512 MiB write) between timed steps, outside the events.
+Barrier + synchronize on both sides of the timed loop; the max over ranks is reported.
+With torchrun (N > 1) every rank runs its own replica of the workload (weak scaling: the
+path shards over (batch, kv head) with no exchange).
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build) on a bounded
+sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s & % bf16 TC peak; softmax/decode HBM GB/s & % of 8 TB/s"
+
+WORKLOADS = {
+    "gqa_causal_prefill": dict(kind="attn", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128, causal=True,
+                               dtype="bf16",
+                               desc="batched GQA causal prefill B=2 Hq=32 Hkv=8 Sq=Sk=4096 D=128 bf16 [B,H,S,D]"),
+    "single_head_4096_bf16": dict(kind="attn", B=1, Hq=1, Hkv=1, Sq=4096, Sk=4096, D=64, causal=False,
+                                  dtype="bf16", desc="single-head attention M=N=4096 d=64 bf16"),
+    "single_head_4096_f32": dict(kind="attn", B=1, Hq=1, Hkv=1, Sq=4096, Sk=4096, D=64, causal=False,
+                                 dtype="f32", desc="single-head attention M=N=4096 d=64 fp32"),
+    "single_head_m64_n100": dict(kind="solve", M=64, N=100, d=32, dtype="f32",
+                                 desc="single-head attention solve M=64 N=100 d=32 fp32"),
+    "gqa_decode": dict(kind="attn", B=8, Hq=32, Hkv=8, Sq=1, Sk=32768, D=128, causal=False, dtype="bf16",
+                       desc="GQA decode B=8 Hq=32 Hkv=8 Sq=1 Sk=32768 D=128 bf16, split-K + LSE combine"),
+    "softmax_rows": dict(kind="softmax", rows=4096, T=32768,
+                         desc="row softmax fp32 [4096, 32768], 8*N(0,1) + one +30 spike per row"),
+    "softmax_1d": dict(kind="softmax", rows=1, T=1 << 26,
+                       desc="1-D softmax fp32 N=2^26, 8*N(0,1) + one +30 spike"),
+}
+DEFAULT = "gqa_causal_prefill"
+
+# Fallback peaks (one earlier GB300 measurement) when the measured-peaks file is absent.
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+# FP32 FMA peak for the CUDA-core paths: 152 SMs x 128 FMA lanes x 2 flop x max SM clock.
+SM_COUNT_GB300 = 152
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture) of
+# each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
+# source that changed since the capture reports null.
+TRAFFIC = {}
+
+
+def peaks():
+    p = dict(FALLBACK)
+    src = "fallback"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "sm_max_mhz"):
+            if k in m:
+                p[k] = float(m[k])
+        src = "measured"
+    except (OSError, ValueError):
+        pass
+    return p, src
+
+
+def work_units(w):
+    """(algorithmic amount per step, unit, roofline bound)."""
+    if w["kind"] == "solve":
+        return 4.0 * w["M"] * w["N"] * w["d"] / 1e12, "TFLOP/s", "alu"
+    if w["kind"] == "attn":
+        if w["Sq"] == 1:  # decode: every K/V byte read once, plus Q and O
+            es = 2 if w["dtype"] == "bf16" else 4
+            b = es * (2 * w["B"] * w["Hkv"] * w["Sk"] * w["D"] + 2 * w["B"] * w["Hq"] * w["D"])
+            return b / 1e9, "GB/s", "hbm"
+        f = 4.0 * w["B"] * w["Hq"] * w["Sq"] * w["Sk"] * w["D"]
+        if w["causal"]:
+            f /= 2
+        return f / 1e12, "TFLOP/s", ("tensor" if w["dtype"] == "bf16" else "alu")
+    # softmax: on-chip rows read once and write once; longer rows read twice
+    per = 8 if w["T"] <= 32768 else 12
+    return per * w["rows"] * w["T"] / 1e9, "GB/s", "hbm"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- inputs
+def make_inputs(name, w, seed=0):
+    import seeded_inputs as si
+    if w["kind"] == "solve":
+        return si.qkv((w["M"], w["d"]), (w["N"], w["d"]), seed)
+    if w["kind"] == "attn":
+        return si.qkv((w["B"], w["Hq"], w["Sq"], w["D"]), (w["B"], w["Hkv"], w["Sk"], w["D"]), seed,
+                      dtype=w["dtype"])
+    return (si.softmax_rows_input(w["rows"], w["T"], seed),)
+
+
+def host_tensors(w, arrays, pin):
+    import torch
+    out = []
+    for a in arrays:
+        if a.dtype == np.uint16:
+            t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(a)
+        out.append(t.pin_memory() if pin else t)
+    return out
+
+
+class Runner:
+    """Device buffers and one call of the hot path for a workload."""
+
+    def __init__(self, name, w, dev, osf, host):
+        import torch
+        self.w, self.osf, self.dev = w, osf, dev
+        self.host = host
+        self.d_in = [h.to(dev) for h in host]
+        if w["kind"] == "solve":
+            self.out = torch.empty(w["M"], w["d"], device=dev)
+            self.ws = None
+        elif w["kind"] == "attn":
+            self.out = torch.empty_like(self.d_in[0])
+            dt = osf.OSF_BF16 if w["dtype"] == "bf16" else osf.OSF_F32
+            n = osf.osf_attn_workspace_bytes(dt, w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Sk"], w["D"])
+            self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        else:
+            self.out = torch.empty_like(self.d_in[0])
+            n = osf.osf_softmax_workspace_bytes(w["rows"], w["T"])
+            self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+
+    def call(self):
+        w, osf = self.w, self.osf
+        if w["kind"] == "solve":
+            q, k, v = self.d_in
+            osf.osf_attn_fwd(q, k, v, self.out, w["M"], w["N"], w["d"])
+        elif w["kind"] == "attn":
+            q, k, v = self.d_in
+            osf.osf_attn_fwd_gqa(q, k, v, out=self.out, causal=w["causal"], workspace=self.ws)
+        else:
+            osf.osf_softmax_rows(self.d_in[0], self.out, workspace=self.ws)
+
+    def call_e2e(self):
+        """Host buffers in, host buffer out: H2D copies, the call, D2H copy of the result."""
+        for d, h in zip(self.d_in, self.host):
+            d.copy_(h, non_blocking=True)
+        self.call()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(h.numel() * h.element_size() for h in self.host)
+
+    def d2h_bytes(self):
+        return self.out.numel() * self.out.element_size()
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (100 ms) kept only while the timed region is open."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+        if vis:  # nvidia-smi numbers physical GPUs; map the visible ordinal back to one
+            ids = [v.strip() for v in vis.split(",") if v.strip()]
+            if index < len(ids):
+                index = ids[index]
+        self.index = index
+        self.samples = []
+        self.open = False
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if self.open:
+                self.samples.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- timing
+def time_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
+    """Per-step CUDA-event times (ms) of ``fn`` on ``stream``, L2 flushed between steps."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.open = True
+    t0 = time.perf_counter()
+    for i in range(steps):
+        if flush is not None:
+            flush.add_(1)
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if sampler:
+        sampler.open = False
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
+
+
+def measure(name, w, osf, dev, steps, warmup, flush, barrier=None, sampler=None, e2e=True):
+    import torch
+    arrays = make_inputs(name, w)
+    host = host_tensors(w, arrays, pin=True)
+    r = Runner(name, w, dev, osf, host)
+    stream = torch.cuda.current_stream(dev)
+    amount, unit, bound = work_units(w)
+    n0 = osf.osf_launch_count()
+    r.call()
+    torch.cuda.synchronize()
+    launches_per_call = osf.osf_launch_count() - n0
+    n1 = osf.osf_launch_count()
+    ms, wall = time_steps(r.call, steps, warmup, flush, stream, barrier, sampler)
+    launches = osf.osf_launch_count() - n1 - warmup * launches_per_call
+    status = osf.osf_device_status()
+    res = {"name": name, "amount": amount, "unit": unit, "bound": bound, "ms": ms, "wall_s": wall,
+           "launches": int(launches), "launches_per_call": int(launches_per_call), "status": status}
+    if e2e:
+        ems, _ = time_steps(r.call_e2e, max(3, steps // 4), 2, flush, stream, barrier)
+        res["e2e_ms"] = ems
+        res["h2d"] = r.h2d_bytes()
+        res["d2h"] = r.d2h_bytes()
+    del r
+    torch.cuda.empty_cache()
+    return res
+
+
+def roofline(res, pk, w):
+    mean_ms = statistics.mean(res["ms"])
+    achieved = res["amount"] / (mean_ms / 1e3)
+    if res["bound"] == "tensor":
+        peak, unit = pk["bf16_tflops"], "TFLOP/s"
+    elif res["bound"] == "hbm":
+        peak, unit = pk["hbm_gbs"], "GB/s"
+    else:  # FP32 FMA pipe
+        peak, unit = SM_COUNT_GB300 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12, "TFLOP/s"
+    t = TRAFFIC.get(res["name"])
+    traffic = None
+    if t and source_hash(os.path.join(ROOT, t["source"])) == t["sha"]:
+        traffic = t["bytes"]
+    return {"bound": res["bound"], "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic": round(res["amount"] * (1e12 if unit == "TFLOP/s" else 1e9)),
+            "per": "flop" if unit == "TFLOP/s" else "byte"}
+
+
+# ------------------------------------------------------------------------------ oracle arm
+def oracle_timed(name, w, budget_s):
+    """Like oracle_sample but with input generation outside the clock."""
+    import oracle
+    import seeded_inputs as si
+    amount, unit, _ = work_units(w)
+    cores = os.cpu_count() or 1
+    elapsed, done, n = 0.0, 0.0, 0
+    if w["kind"] == "solve":
+        Q, K, V = make_inputs(name, w)
+        while elapsed < min(budget_s, 2.0):
+            t = time.perf_counter()
+            oracle.attention(Q, K, V)
+            elapsed += time.perf_counter() - t
+            n += 1
+            done += amount
+        return done / elapsed, unit, f"{n} full solves", cores
+    if w["kind"] == "attn" and w["Sq"] > 1:
+        B, Hq, S, D = w["B"], w["Hq"], w["Sq"], w["D"]
+        per_head = amount / (B * Hq)
+        while n < B * Hq and elapsed < budget_s:
+            q = si.normal_f32((S, D), n, si.STREAM_Q)
+            kk = si.normal_f32((w["Sk"], D), n, si.STREAM_K)
+            vv = si.normal_f32((w["Sk"], D), n, si.STREAM_V)
+            if w["dtype"] == "bf16":
+                q, kk, vv = (si.bf16_bits_to_f32(si.f32_to_bf16_bits(a)) for a in (q, kk, vv))
+            t = time.perf_counter()
+            oracle.attention(q, kk, vv, causal=w["causal"])
+            elapsed += time.perf_counter() - t
+            n += 1
+            done += per_head
+        return done / elapsed, unit, f"{n} of {B * Hq} (b, q-head) problems, full {S}x{w['Sk']} scores each", cores
+    if w["kind"] == "attn":
+        B, Hq, Hkv, Sk, D = w["B"], w["Hq"], w["Hkv"], w["Sk"], w["D"]
+        G = Hq // Hkv
+        per = amount / (B * Hkv)
+        while n < B * Hkv and elapsed < budget_s:
+            q = si.normal_f32((1, G, 1, D), n, si.STREAM_Q)
+            kk = si.normal_f32((1, 1, Sk, D), n, si.STREAM_K)
+            vv = si.normal_f32((1, 1, Sk, D), n, si.STREAM_V)
+            t = time.perf_counter()
+            oracle.attention_gqa(q, kk, vv)
+            elapsed += time.perf_counter() - t
+            n += 1
+            done += per
+        return done / elapsed, unit, f"{n} of {B * Hkv} (b, kv-head) groups", cores
+    rows, T = w["rows"], w["T"]
+    step = 64 if rows > 1 else 1
+    while n < rows and elapsed < budget_s:
+        x = si.softmax_rows_input(step, T, n)
+        t = time.perf_counter()
+        oracle.softmax(x)
+        elapsed += time.perf_counter() - t
+        n += step
+        done += amount * step / rows
+    return done / elapsed, unit, f"{n} of {rows} rows of {T}", cores
+
+
+# ------------------------------------------------------------------------------ main
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reference_arm(args, world, rank):
+    w = WORKLOADS[args.workload]
+    if rank != 0:
+        return 0
+    vals = []
+    sample = cores = unit = None
+    for _ in range(args.warmup):
+        oracle_timed(args.workload, w, args.ref_budget / 4)
+    for _ in range(args.steps):
+        v, unit, sample, cores = oracle_timed(args.workload, w, args.ref_budget)
+        vals.append(v)
+    value = statistics.median(vals)
+    amount, _, _ = work_units(w)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": amount / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w["desc"], "oracle": "fp64 numpy three-pass"},
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": unit, "cores": cores,
+                             "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="osf", choices=["osf", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-suite", action="store_true", help="skip the other workloads")
+    ap.add_argument("--suite-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time (cpu_baseline)")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds per reference-arm step")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    import online_softmax_flash_gb300 as osf
+    from online_softmax_flash_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        dist.barrier()
+        if rank != 0:
+            _build.build()
+        barrier = dist.barrier
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    osf.lib()
+    pk, pk_src = peaks()
+    flush = torch.empty(128 << 20, dtype=torch.float32, device=dev)  # 512 MiB > L2
+
+    w = WORKLOADS[args.workload]
+    sampler = ClockSampler(local)
+    sampler.start()
+    res = measure(args.workload, w, osf, dev, args.steps, args.warmup, flush, barrier, sampler)
+    sampler.stop()
+    mean_ms = statistics.mean(res["ms"])
+    total_ms = sum(res["ms"])
+    e2e_ms = statistics.mean(res["e2e_ms"])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+        mean_ms = total_ms / args.steps
+    value = world * res["amount"] / (mean_ms / 1e3)
+    rl = roofline(res, pk, w)
+    rl["peak_source"] = pk_src + (" burst" if rl["bound"] == "tensor" else "")
+
+    suite = {}
+    if not args.no_suite:
+        for name, ww in WORKLOADS.items():
+            if name == args.workload:
+                continue
+            r2 = measure(name, ww, osf, dev, args.suite_steps, 3, flush, barrier, None, e2e=False)
+            m2 = statistics.mean(r2["ms"])
+            suite[name] = {"workload": ww["desc"], "value": round(r2["amount"] / (m2 / 1e3), 3),
+                           "unit": r2["unit"], "ms_per_step": round(m2, 5),
+                           "roofline": roofline(r2, pk, ww), "launches_per_call": r2["launches_per_call"],
+                           "device_status": r2["status"]}
+
+    cpu = None
+    if rank == 0:
+        v, unit, sample, cores = oracle_timed(args.workload, w, args.cpu_budget)
+        cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": res["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.get("dtype", "f32"), "data": "synthetic",
+            "config": {"workload": w["desc"], "l2": "flushed (512 MiB write) between timed steps",
+                       "inputs": "seeded i.i.d. N(0,1) (SplitMix64 + Box-Muller), resident in HBM",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": rl, "cpu_baseline": cpu,
+            "e2e": {"value": round(world * res["amount"] / (e2e_ms / 1e3), 3), "unit": res["unit"],
+                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                    "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": res["launches"], "launches_per_step": res["launches_per_call"],
+            "device_status": res["status"], "clocks": sampler.summary(), "suite": suite,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,152 @@
+/*
+ * osf.h -- C ABI of libosf: single-pass (online-softmax) attention and streaming softmax
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [SA] "softmax_attention" (blog.euler0525.cn/posts/3fb3592b), "实现思路" and "附录":
+ *        solve(Q, K, V, output, M, N, d) on row-major [M,d] / [N,d] tensors already on the GPU,
+ *        scale d^-0.5, keys streamed in blocks with a running max / rescale / denominator /
+ *        numerator, -inf for keys past N.
+ *   [Q3] "从零开始写Qwen3（五-其一）使用Triton实现自注意力" (gitcode.csdn.net), "自注意力原理",
+ *        "多头自注意力", "stride的作用", "GQA": O = softmax(mask(QK^T/sqrt(D)))V on [B,H,S,D]
+ *        tensors, Hq divisible by Hkv, kv head = q head // (Hq/Hkv), causal tril mask applied
+ *        only when the query length is > 1.
+ *   [TP] Triton-Puzzles write-up (fadingcoder.top/post/105980), "Puzzle 8: Long Softmax":
+ *        softmax of each row of a [rows, T] matrix; two-loop online form.
+ *   [SO] "Softmax 算子的实现与优化" (blog.euler0525.cn/posts/5db73590), "Online Softmax" and
+ *        "CUDA 版本": the boxed (m, l) recurrence; extern "C" solve(const float* input,
+ *        float* output, int N) on device pointers, returning without work when N <= 0.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) on the current device,
+ *     except where a parameter says otherwise.  The caller owns every buffer; the library
+ *     never allocates or frees device memory in these calls.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and the call returns without
+ *     waiting (unlike [SO]'s solve, which synchronises the device).  A returned OSF_OK means
+ *     the arguments were valid and the launches were accepted.
+ *   - Layouts are contiguous row-major: [M,d], [N,d], [B,H,S,D] (D fastest), [rows,T].
+ *   - Return value: an osf_status code.  No entry point traps or asserts on the device.
+ *     Device-side failures (a bounded wait that ran out) are recorded in a device status word
+ *     read by osf_device_status().
+ *   - Thread safety: entry points may be called concurrently from several host threads on
+ *     different streams; calls sharing a workspace buffer must be ordered by the caller.
+ */
+#ifndef OSF_H
+#define OSF_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *osf_stream;
+
+typedef enum osf_status {
+    OSF_OK = 0,
+    OSF_ERR_INVALID = 1,     /* invalid argument: NULL with non-zero size, negative size,
+                                Hq % Hkv != 0, causal with 1 < Sq != Sk, forbidden aliasing */
+    OSF_ERR_UNSUPPORTED = 2, /* valid but outside what the library implements (e.g. D > 256,
+                                or a size whose element count exceeds 2^31 per head) */
+    OSF_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    OSF_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (osf_device_status) */
+    OSF_ERR_WORKSPACE = 5    /* workspace NULL or smaller than the *_workspace_bytes query */
+} osf_status;
+
+typedef enum osf_dtype {
+    OSF_F32 = 0,   /* IEEE float32 inputs and outputs */
+    OSF_BF16 = 1   /* bfloat16 Q/K/V/O; accumulation and softmax state in float32 */
+} osf_dtype;
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char *osf_status_string(int status);
+
+/* Library ABI version, major * 10000 + minor * 100 + patch. */
+int osf_version(void);
+
+/*
+ * osf_attn_fwd -- single-head attention, [SA] "实现思路" / "附录" solve(Q, K, V, output, M, N, d):
+ *     out[i, :] = sum_j softmax_j(Q[i,:] . K[j,:] * d^-0.5) V[j, :]
+ * Q: [M, d] float32, K: [N, d], V: [N, d], out: [M, d]; all row-major contiguous, device.
+ * M == 0 or N == 0: returns OSF_OK and touches nothing (the pages return early on empty input).
+ * d must be 1..256 (OSF_ERR_UNSUPPORTED above).  out must not overlap Q, K or V.
+ */
+int osf_attn_fwd(const float *Q, const float *K, const float *V, float *out,
+                 int M, int N, int d, osf_stream stream);
+
+/*
+ * osf_attn_fwd_gqa -- batched grouped-query attention with optional causal mask,
+ * [Q3] "自注意力原理" + "GQA":
+ *     O[b,h,i,:] = sum_j softmax_j(mask(Q[b,h,i,:] . K[b,h/G,j,:] * scale)) V[b,h/G,j,:]
+ *     G = Hq / Hkv.  mask: when causal && Sq > 1, key j is excluded for j > i (top-left
+ *     aligned tril(ones(Sq, Sk))); when Sq == 1 every key is used, as on the page.
+ * Q: [B, Hq, Sq, D], K and V: [B, Hkv, Sk, D], O: [B, Hq, Sq, D], all of `dtype`.
+ * scale <= 0 selects D^-0.5.
+ * lse: optional (NULL) float32 [B, Hq, Sq] receiving the natural-log log-sum-exp of each row's
+ *      scaled, masked scores (m + ln l).
+ * workspace: device scratch for split-K partial states; query the size with
+ *      osf_attn_workspace_bytes (may be 0, then workspace may be NULL).
+ * Sq == 0 or Sk == 0 or B == 0: OSF_OK, nothing written.  Hq % Hkv != 0, causal with
+ * Sq > 1 && Sq != Sk, or O overlapping Q/K/V: OSF_ERR_INVALID.  D must be 1..256.
+ * Kernel choice (internal): bf16 with D in {64, 128} and Sq > 1 runs the tensor-core
+ * (tcgen05/TMEM/TMA) prefill kernel; Sq == 1 runs the split-K decode kernel followed by a
+ * log-sum-exp combine; everything else runs the general CUDA-core kernel.
+ */
+int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int dtype,
+                     int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                     float *lse, void *workspace, size_t workspace_bytes, osf_stream stream);
+
+/* Bytes of workspace osf_attn_fwd_gqa needs for these arguments (written to *bytes). */
+int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                             size_t *bytes);
+
+/*
+ * osf_attn_decode_gqa -- the Sq == 1 path of osf_attn_fwd_gqa with an explicit split count.
+ * The Sk keys of each (b, kv head) are cut into `num_splits` contiguous chunks; each chunk
+ * yields a partial state (m_s, l_s, acc_s) and a combine step merges them with the
+ * log-sum-exp rule (the [SO] "Online Softmax" recurrence applied to whole partial states;
+ * the pages do not describe the split itself).  num_splits <= 0 picks a count from the SM
+ * count.  Q: [B, Hq, 1, D], K/V: [B, Hkv, Sk, D], O: [B, Hq, 1, D].  Workspace size:
+ * osf_attn_decode_workspace_bytes with the same num_splits.
+ */
+int osf_attn_decode_gqa(const void *Q, const void *K, const void *V, void *O, int dtype,
+                        int B, int Hq, int Hkv, int Sk, int D, float scale, float *lse,
+                        int num_splits, void *workspace, size_t workspace_bytes,
+                        osf_stream stream);
+int osf_attn_decode_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sk, int D,
+                                    int num_splits, size_t *bytes);
+
+/*
+ * osf_softmax_rows -- row softmax, [TP] "Puzzle 8: Long Softmax" / [SO] "Online Softmax":
+ *     z[r, j] = exp(x[r, j] - m_r) / l_r,  m_r = max_j x[r, j],  l_r = sum_j exp(x[r, j] - m_r)
+ * x, z: [rows, T] float32 row-major, device.  z == x (in place) is allowed; any other overlap
+ * is OSF_ERR_INVALID.  rows == 0 or T == 0: OSF_OK, nothing written.
+ * Rows of up to 32768 elements are held on chip (one read, one write); longer rows -- e.g.
+ * one 1-D vector, rows == 1 -- are cut into chunks processed by many CTAs, whose partial
+ * (m, l) states are merged and followed by a normalising pass (two reads, one write).  That
+ * path needs workspace: osf_softmax_workspace_bytes (0 when not needed).
+ */
+int osf_softmax_rows(const float *x, float *z, long long rows, long long T,
+                     void *workspace, size_t workspace_bytes, osf_stream stream);
+int osf_softmax_workspace_bytes(long long rows, long long T, size_t *bytes);
+
+/*
+ * osf_device_status -- synchronise `stream`, then return (and reset to OSF_OK) the device
+ * status word of the current device: OSF_ERR_TIMEOUT if any kernel gave up a bounded wait
+ * since the last call, OSF_ERR_CUDA if the synchronisation itself failed, else OSF_OK.
+ */
+int osf_device_status(osf_stream stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int osf_sm_count(void);
+
+/* Total number of kernels this library has launched in this process (all devices, all
+ * threads); a diagnostic for counting launches in a timed region. */
+unsigned long long osf_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSF_H */

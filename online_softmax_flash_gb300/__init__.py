@@ -1,0 +1,215 @@
+"""Python binding of libosf (include/osf.h): same entry-point names, argument marshalling only.
+
+Every step of attention and softmax runs in libosf's CUDA kernels.  PyTorch supplies device
+memory and the current CUDA stream.  There is no fallback: if libosf.so is missing or a
+tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "OSF_OK", "OSF_ERR_INVALID", "OSF_ERR_UNSUPPORTED", "OSF_ERR_CUDA", "OSF_ERR_TIMEOUT",
+    "OSF_ERR_WORKSPACE", "OSF_F32", "OSF_BF16", "OsfError", "lib", "library_path",
+    "osf_status_string", "osf_version", "osf_sm_count", "osf_attn_fwd", "osf_attn_fwd_gqa",
+    "osf_attn_workspace_bytes", "osf_attn_decode_gqa", "osf_attn_decode_workspace_bytes",
+    "osf_softmax_rows", "osf_softmax_workspace_bytes", "osf_device_status", "osf_launch_count",
+    "solve",
+]
+
+OSF_OK, OSF_ERR_INVALID, OSF_ERR_UNSUPPORTED, OSF_ERR_CUDA, OSF_ERR_TIMEOUT, OSF_ERR_WORKSPACE = range(6)
+OSF_F32, OSF_BF16 = 0, 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libosf.so")
+_lib = None
+
+_vp, _sz, _i, _ll, _f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+_SIGS = {
+    "osf_status_string": (ctypes.c_char_p, [_i]),
+    "osf_version": (_i, []),
+    "osf_sm_count": (_i, []),
+    "osf_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "osf_attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
+    "osf_attn_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "osf_attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
+    "osf_attn_decode_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "osf_softmax_rows": (_i, [_vp, _vp, _ll, _ll, _vp, _sz, _vp]),
+    "osf_softmax_workspace_bytes": (_i, [_ll, _ll, ctypes.POINTER(_sz)]),
+    "osf_device_status": (_i, [_vp]),
+    "osf_launch_count": (ctypes.c_ulonglong, []),
+}
+
+
+class OsfError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {osf_status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libosf.so (built by ``_build.build()``); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"libosf.so not found at {library_path}: build it first "
+                               "(online_softmax_flash_gb300._build.build())")
+        l = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != OSF_OK:
+        raise OsfError(status, where)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(dev) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _need_cuda(*ts) -> None:
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libosf works on CUDA tensors only (no CPU path)")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("libosf expects contiguous row-major tensors")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return OSF_F32
+    if t.dtype == torch.bfloat16:
+        return OSF_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def osf_status_string(status: int) -> str:
+    return lib().osf_status_string(int(status)).decode()
+
+
+def osf_version() -> int:
+    return lib().osf_version()
+
+
+def osf_sm_count() -> int:
+    return lib().osf_sm_count()
+
+
+def osf_attn_fwd(Q, K, V, out, M: int, N: int, d: int) -> None:
+    """out[M, d] = softmax(Q K^T / sqrt(d)) V for float32 Q[M, d], K[N, d], V[N, d]."""
+    _need_cuda(Q, K, V, out)
+    _check(lib().osf_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), M, N, d, _stream(Q.device)),
+           "osf_attn_fwd")
+
+
+def solve(Q, K, V, output, M: int, N: int, d: int) -> None:
+    """The pages' ``solve(Q, K, V, output, M, N, d)``: osf_attn_fwd, then wait for it."""
+    osf_attn_fwd(Q, K, V, output, M, N, d)
+    torch.cuda.current_stream(Q.device).synchronize()
+
+
+def osf_attn_workspace_bytes(dtype: int, B, Hq, Hkv, Sq, Sk, D) -> int:
+    n = _sz(0)
+    _check(lib().osf_attn_workspace_bytes(dtype, B, Hq, Hkv, Sq, Sk, D, ctypes.byref(n)),
+           "osf_attn_workspace_bytes")
+    return n.value
+
+
+def _workspace(nbytes: int, dev, workspace):
+    if nbytes == 0:
+        return workspace
+    if workspace is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    return workspace
+
+
+def osf_attn_fwd_gqa(q, k, v, out=None, causal: bool = False, scale: float | None = None,
+                     lse=None, workspace=None):
+    """Grouped-query attention on [B, H, S, D] tensors; returns ``out`` (allocated if None)."""
+    _need_cuda(q, k, v, out, lse)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_n = osf_attn_workspace_bytes(dt, B, Hq, Hkv, Sq, Sk, D)
+    ws = _workspace(ws_n, q.device, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().osf_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), dt, B, Hq, Hkv, Sq, Sk, D,
+                                  int(bool(causal)), 0.0 if scale is None else float(scale),
+                                  _ptr(lse), _ptr(ws), ws_bytes, _stream(q.device)),
+           "osf_attn_fwd_gqa")
+    return out
+
+
+def osf_attn_decode_workspace_bytes(dtype: int, B, Hq, Hkv, Sk, D, num_splits: int = 0) -> int:
+    n = _sz(0)
+    _check(lib().osf_attn_decode_workspace_bytes(dtype, B, Hq, Hkv, Sk, D, num_splits, ctypes.byref(n)),
+           "osf_attn_decode_workspace_bytes")
+    return n.value
+
+
+def osf_attn_decode_gqa(q, k, v, out=None, scale: float | None = None, lse=None,
+                        num_splits: int = 0, workspace=None):
+    """Sq == 1 attention with an explicit split count over the keys."""
+    _need_cuda(q, k, v, out, lse)
+    B, Hq, Sq, D = q.shape
+    if Sq != 1:
+        raise ValueError("osf_attn_decode_gqa expects q of shape [B, Hq, 1, D]")
+    Hkv, Sk = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_n = osf_attn_decode_workspace_bytes(dt, B, Hq, Hkv, Sk, D, num_splits)
+    ws = _workspace(ws_n, q.device, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().osf_attn_decode_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), dt, B, Hq, Hkv, Sk, D,
+                                     0.0 if scale is None else float(scale), _ptr(lse),
+                                     int(num_splits), _ptr(ws), ws_bytes, _stream(q.device)),
+           "osf_attn_decode_gqa")
+    return out
+
+
+def osf_softmax_workspace_bytes(rows: int, T: int) -> int:
+    n = _sz(0)
+    _check(lib().osf_softmax_workspace_bytes(rows, T, ctypes.byref(n)), "osf_softmax_workspace_bytes")
+    return n.value
+
+
+def osf_softmax_rows(x, z=None, workspace=None):
+    """Row softmax of a float32 [rows, T] (or 1-D [T]) tensor; ``z is x`` runs in place."""
+    _need_cuda(x, z)
+    if x.dtype != torch.float32:
+        raise ValueError("osf_softmax_rows takes float32")
+    T = x.shape[-1] if x.dim() > 0 else 1
+    rows = x.numel() // T if T else 0
+    if z is None:
+        z = torch.empty_like(x)
+    ws_n = osf_softmax_workspace_bytes(rows, T)
+    ws = _workspace(ws_n, x.device, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().osf_softmax_rows(_ptr(x), _ptr(z), rows, T, _ptr(ws), ws_bytes, _stream(x.device)),
+           "osf_softmax_rows")
+    return z
+
+
+def osf_launch_count() -> int:
+    """Kernels launched by libosf so far in this process."""
+    return lib().osf_launch_count()
+
+
+def osf_device_status() -> int:
+    """Synchronise the current stream and return (and clear) the device status word."""
+    return lib().osf_device_status(_stream(torch.cuda.current_device()))

@@ -1,0 +1,301 @@
+// General CUDA-core attention forward: any head dim 1..256, float32 or bfloat16 inputs, GQA,
+// optional causal mask, optional split over the key range with a log-sum-exp combine.
+//
+// The recurrence is the one of "softmax_attention" (blog.euler0525.cn/posts/3fb3592b), section
+// "实现思路": keys are streamed in blocks; per query row a running max m, a rescale factor
+// alpha = exp(m_prev - m), a denominator l and a numerator acc are carried, and the row is
+// acc / l at the end, so the [M, N] score matrix never leaves the chip.  Keys past the end of
+// the sequence (and, with the causal mask of "从零开始写Qwen3（五-其一）...", "自注意力原理",
+// keys after the query) score -inf, never 0.
+//
+// Unlike the page's one-program-per-query kernel, a CTA owns a tile of BM query rows and
+// BN = 64 keys at a time, so every K/V element loaded into shared memory is reused by BM rows;
+// S = Q K^T and O += P V are register-tiled 4 x 4 outer products on the FMA pipe.  Scores are
+// kept in base 2 (scale * log2 e folded into one multiplier) so each exponential is one ex2.
+#include "osf_internal.cuh"
+
+namespace osf {
+namespace {
+
+constexpr int BN = 64;  // keys per tile
+
+template <int DP, int BM>
+struct SimtCfg {
+    static constexpr int THREADS = BM * 4;             // (BM/4) row groups x 16 column groups
+    static constexpr int QS = BM + 4;                  // padded length of a transposed Q column
+    static constexpr int KS = BN + 4;                  // padded length of a transposed K column
+    static constexpr int OC = DP / 16;                 // O columns per thread
+    static constexpr int VEC = OC < 4 ? OC : 4;        // contiguous O columns per chunk
+    static constexpr int NCH = OC / VEC;               // chunks of VEC columns
+    static constexpr int SMEM_FLOATS = DP * QS + DP * KS + BN * DP + BN * QS;
+    static constexpr size_t SMEM_BYTES = size_t(SMEM_FLOATS) * sizeof(float);
+};
+
+template <typename T>
+__device__ __forceinline__ float ld(const T *p) { return to_f32(*p); }
+
+template <typename T, int DP, int BM>
+__global__ void __launch_bounds__(BM * 4)
+attn_simt_kernel(const AttnProblem p) {
+    using C = SimtCfg<DP, BM>;
+    extern __shared__ __align__(16) float smem[];
+    float *Qs = smem;                    // [DP][QS]  Q tile, transposed
+    float *Ks = Qs + DP * C::QS;         // [DP][KS]  K tile, transposed
+    float *Vs = Ks + DP * C::KS;         // [BN][DP]  V tile
+    float *Ps = Vs + BN * DP;            // [BN][QS]  P tile, transposed
+
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;             // key group (S) / column group (O)
+    const int ty = tid >> 4;             // row group: rows ty*4 .. ty*4+3
+
+    const int n_qt = (p.Sq + BM - 1) / BM;
+    // causal: heaviest (last) query tiles first
+    const int qt = p.causal ? (n_qt - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int bh = blockIdx.y;           // b * Hq + hq
+    const int split = blockIdx.z;
+    const int b = bh / p.Hq, hq = bh % p.Hq;
+    const int kvh = hq / (p.Hq / p.Hkv);
+    const int q0 = qt * BM;
+    const int D = p.D;
+
+    const T *Qg = static_cast<const T *>(p.q) + ((size_t)bh * p.Sq + q0) * D;
+    const T *Kg = static_cast<const T *>(p.k) + ((size_t)b * p.Hkv + kvh) * (size_t)p.Sk * D;
+    const T *Vg = static_cast<const T *>(p.v) + ((size_t)b * p.Hkv + kvh) * (size_t)p.Sk * D;
+
+    // key range of this split: a fixed partition of [0, Sk) in whole tiles, clipped by causality
+    const int n_kt_all = (p.Sk + BN - 1) / BN;
+    const int tps = (n_kt_all + p.splits - 1) / p.splits;
+    const int k_begin = split * tps * BN;
+    int k_end = min(p.Sk, (split + 1) * tps * BN);
+    if (p.causal) k_end = min(k_end, q0 + BM);
+
+    for (int idx = tid; idx < BM * DP; idx += C::THREADS) {
+        const int r = idx / DP, d = idx % DP;
+        Qs[d * C::QS + r] = (q0 + r < p.Sq && d < D) ? ld(Qg + (size_t)r * D + d) : 0.f;
+    }
+
+    float m[4], l[4], acc[4][C::OC];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < C::OC; ++c) acc[i][c] = 0.f;
+    }
+
+    for (int kt0 = k_begin; kt0 < k_end; kt0 += BN) {
+        __syncthreads();  // previous tile's K/V/P fully consumed (and Q stored, first time)
+        for (int idx = tid; idx < BN * DP; idx += C::THREADS) {
+            const int c = idx / DP, d = idx % DP;
+            const bool ok = (kt0 + c < k_end) && d < D;
+            const size_t off = (size_t)(kt0 + c) * D + d;
+            Ks[d * C::KS + c] = ok ? ld(Kg + off) : 0.f;
+            Vs[c * DP + d] = ok ? ld(Vg + off) : 0.f;
+        }
+        __syncthreads();
+
+        // S = Q K^T for rows ty*4.., keys tx*4..
+        float s[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < DP; ++d) {
+            const float4 a = *reinterpret_cast<const float4 *>(&Qs[d * C::QS + ty * 4]);
+            const float4 k4 = *reinterpret_cast<const float4 *>(&Ks[d * C::KS + tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s[i][j] = fmaf(av[i], kv[j], s[i][j]);
+        }
+
+        // scale (base 2), mask, online max / rescale / denominator
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = q0 + ty * 4 + i;
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int key = kt0 + tx * 4 + j;
+                const bool valid = key < k_end && (!p.causal || key <= row);
+                s[i][j] = valid ? s[i][j] * p.scale_log2 : -INFINITY;
+                tmax = fmaxf(tmax, s[i][j]);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            const float m_new = fmaxf(m[i], tmax);
+            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;   // fully masked so far
+            const float alpha = ex2_approx(m[i] - m_ref);
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                s[i][j] = ex2_approx(s[i][j] - m_ref);
+                rs += s[i][j];
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+            l[i] = l[i] * alpha + rs;
+            m[i] = m_new;
+#pragma unroll
+            for (int c = 0; c < C::OC; ++c) acc[i][c] *= alpha;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<float4 *>(&Ps[(tx * 4 + j) * C::QS + ty * 4]) =
+                make_float4(s[0][j], s[1][j], s[2][j], s[3][j]);
+        }
+        __syncthreads();
+
+        // O += P V
+#pragma unroll 4
+        for (int kk = 0; kk < BN; ++kk) {
+            const float4 a = *reinterpret_cast<const float4 *>(&Ps[kk * C::QS + ty * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int ch = 0; ch < C::NCH; ++ch) {
+                const float *vp = &Vs[kk * DP + ch * 16 * C::VEC + tx * C::VEC];
+                float vv[C::VEC];
+                if constexpr (C::VEC == 4) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(vp);
+                    vv[0] = v4.x; vv[1] = v4.y; vv[2] = v4.z; vv[3] = v4.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < C::VEC; ++e) vv[e] = vp[e];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int e = 0; e < C::VEC; ++e)
+                        acc[i][ch * C::VEC + e] = fmaf(av[i], vv[e], acc[i][ch * C::VEC + e]);
+            }
+        }
+    }
+
+    // epilogue
+    const long long rows_total = (long long)p.B * p.Hq * p.Sq;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = q0 + ty * 4 + i;
+        if (r >= p.Sq) continue;
+        const long long row = (long long)bh * p.Sq + r;
+        if (p.splits == 1) {
+            const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+            T *Og = static_cast<T *>(p.o) + row * D;
+#pragma unroll
+            for (int ch = 0; ch < C::NCH; ++ch)
+#pragma unroll
+                for (int e = 0; e < C::VEC; ++e) {
+                    const int col = ch * 16 * C::VEC + tx * C::VEC + e;
+                    if (col < D) Og[col] = from_f32<T>(acc[i][ch * C::VEC + e] * inv);
+                }
+            if (p.lse && tx == 0)
+                p.lse[row] = l[i] > 0.f ? (m[i] + __log2f(l[i])) * kLn2 : -INFINITY;
+        } else {
+            float *A = p.part_acc + ((size_t)split * rows_total + row) * D;
+#pragma unroll
+            for (int ch = 0; ch < C::NCH; ++ch)
+#pragma unroll
+                for (int e = 0; e < C::VEC; ++e) {
+                    const int col = ch * 16 * C::VEC + tx * C::VEC + e;
+                    if (col < D) A[col] = acc[i][ch * C::VEC + e];
+                }
+            if (tx == 0) {
+                p.part_m[(size_t)split * rows_total + row] = m[i];
+                p.part_l[(size_t)split * rows_total + row] = l[i];
+            }
+        }
+    }
+}
+
+// Log-sum-exp combine of split partial states: M = max_s m_s, w_s = 2^(m_s - M),
+// O = sum_s w_s acc_s / sum_s w_s l_s, lse = (M + log2 L) ln 2.  One warp per output row.
+template <typename T>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) {
+    const long long rows_total = (long long)p.B * p.Hq * p.Sq;
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows_total) return;
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.part_m[(size_t)s * rows_total + row]);
+    const float Mref = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+    for (int s = 0; s < p.splits; ++s)
+        L += p.part_l[(size_t)s * rows_total + row] * ex2_approx(p.part_m[(size_t)s * rows_total + row] - Mref);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    T *Og = static_cast<T *>(p.o) + row * p.D;
+    for (int c = lane; c < p.D; c += 32) {
+        float a = 0.f;
+        for (int s = 0; s < p.splits; ++s) {
+            const float w = ex2_approx(p.part_m[(size_t)s * rows_total + row] - Mref);
+            a += w * p.part_acc[((size_t)s * rows_total + row) * p.D + c];
+        }
+        Og[c] = from_f32<T>(a * inv);
+    }
+    if (p.lse && lane == 0) p.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+}
+
+template <typename T, int DP, int BM>
+cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
+    using C = SimtCfg<DP, BM>;
+    static bool configured = false;   // attribute is per function; idempotent, benign race
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, DP, BM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    dim3 grid((p.Sq + BM - 1) / BM, p.B * p.Hq, p.splits);
+    attn_simt_kernel<T, DP, BM><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_dp(const AttnProblem &p, cudaStream_t s) {
+    if (p.D <= 16) return launch_t<T, 16, 64>(p, s);
+    if (p.D <= 32) return launch_t<T, 32, 64>(p, s);
+    if (p.D <= 64) return launch_t<T, 64, 64>(p, s);
+    if (p.D <= 128) return launch_t<T, 128, 64>(p, s);
+    return launch_t<T, 256, 32>(p, s);
+}
+
+int block_m(int D) { return D <= 128 ? 64 : 32; }
+
+}  // namespace
+
+int attn_simt_pick_splits(const AttnProblem &p, int sm_count) {
+    const int BM = block_m(p.D);
+    const long long ctas = (long long)((p.Sq + BM - 1) / BM) * p.B * p.Hq;
+    const int n_kt = (p.Sk + BN - 1) / BN;
+    if (ctas >= 2LL * sm_count || n_kt <= 1) return 1;
+    long long want = (2LL * sm_count + ctas - 1) / ctas;
+    if (want > n_kt) want = n_kt;
+    if (want > 64) want = 64;
+    return (int)want;
+}
+
+size_t attn_simt_partial_floats(int splits, long long rows, int D) {
+    if (splits <= 1) return 0;
+    return (size_t)splits * rows * (size_t)(D + 2);
+}
+
+cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t s) {
+    return p.dtype == OSF_F32 ? launch_dp<float>(p, s) : launch_dp<__nv_bfloat16>(p, s);
+}
+
+cudaError_t launch_attn_combine(const AttnProblem &p, cudaStream_t s) {
+    const long long rows_total = (long long)p.B * p.Hq * p.Sq;
+    const unsigned blocks = (unsigned)((rows_total + 7) / 8);
+    if (p.dtype == OSF_F32)
+        attn_combine_kernel<float><<<blocks, 256, 0, s>>>(p);
+    else
+        attn_combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace osf

@@ -1,0 +1,84 @@
+// Internal declarations shared by libosf's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "osf.h"
+
+namespace osf {
+
+// log2(e): scores are kept in base-2 units, s2 = s * scale * log2(e), so every exponential is a
+// single ex2 (the "exp(x) = exp2(log2(e) * x)" rewrite of the Triton-Puzzles write-up, Puzzle 8).
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status word values (match osf_status).
+constexpr int kStatusTimeout = OSF_ERR_TIMEOUT;
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Merge two (m, l) softmax states (base-2 exponents): the boxed recurrence of
+// "Softmax 算子的实现与优化", "Online Softmax", applied to a partial state instead of one block.
+__device__ __forceinline__ void merge_ml(float &m, float &l, float m2, float l2) {
+    float mn = fmaxf(m, m2);
+    if (mn == -INFINITY) return;  // both empty
+    l = l * ex2_approx(m - mn) + l2 * ex2_approx(m2 - mn);
+    m = mn;
+}
+
+// ---------------------------------------------------------------- attention problem
+struct AttnProblem {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;          // optional [B, Hq, Sq]
+    int dtype;           // OSF_F32 / OSF_BF16
+    int B, Hq, Hkv, Sq, Sk, D;
+    int causal;          // already folded with Sq > 1
+    float scale_log2;    // scale * log2(e)
+    // split-K partial state workspace (float): acc [splits][B*Hq*Sq][D], m/l [splits][B*Hq*Sq]
+    int splits;
+    float *part_acc, *part_m, *part_l;
+    int *status;         // device status word
+};
+
+// Count of kernels launched by the library (diagnostics; see osf_launch_count).
+void count_launches(int n);
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t s);
+cudaError_t launch_attn_combine(const AttnProblem &p, cudaStream_t s);
+size_t attn_simt_partial_floats(int splits, long long rows, int D);
+int attn_simt_pick_splits(const AttnProblem &p, int sm_count);
+
+cudaError_t launch_softmax_rows(const float *x, float *z, long long rows, long long T,
+                                float *ws, int sm_count, cudaStream_t s);
+size_t softmax_workspace_floats(long long rows, long long T, int sm_count);
+
+}  // namespace osf

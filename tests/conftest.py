@@ -39,3 +39,55 @@ def read_golden(name):
             key, *vals = line.split()
             out.setdefault(key, []).append([float(v) for v in vals])
     return out
+
+
+@pytest.fixture(scope="session")
+def osf():
+    """The product binding, with libosf.so built in-tree (builds on first use)."""
+    from online_softmax_flash_gb300 import _build
+    _build.build()
+    import online_softmax_flash_gb300 as m
+    m.lib()
+    return m
+
+
+# Tolerances restated from the problem statement: float32 paths max abs error <= 1e-4;
+# bfloat16 inputs |gpu - ref| <= 2e-2 + 1e-2 |ref| elementwise (abs 2e-2 with rel 1e-2 read as
+# an allclose pair); softmax rows sum to 1 within 1e-5.
+F32_ATOL = 1e-4
+BF16_ATOL, BF16_RTOL = 2e-2, 1e-2
+SUM_TOL = 1e-5
+
+
+def assert_f32_close(got, ref, atol=F32_ATOL, what=""):
+    import numpy as np
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    assert err <= atol, f"{what}: max abs error {err:.3e} > {atol:.1e}"
+    return err
+
+
+def assert_bf16_close(got, ref, what=""):
+    import numpy as np
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    excess = np.abs(got - ref) - (BF16_ATOL + BF16_RTOL * np.abs(ref))
+    worst = float(np.max(excess)) if got.size else -1.0
+    assert worst <= 0, (f"{what}: tolerance exceeded by {worst:.3e} "
+                        f"(max abs err {float(np.max(np.abs(got - ref))):.3e})")
+    return float(np.max(np.abs(got - ref))) if got.size else 0.0
+
+
+def bf16_tensor(bits, device="cuda"):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def f32_tensor(a, device="cuda"):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)

@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every function that
+include/osf.h declares, and rejects invalid arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "osf.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(osf_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("osf_attn_fwd", "osf_attn_fwd_gqa", "osf_softmax_rows", "osf_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(osf):
+    lib = ctypes.CDLL(osf.library_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in osf.h but not exported: {missing}"
+
+
+def test_status_strings(osf):
+    for code in range(6):
+        s = osf.osf_status_string(code)
+        assert s.startswith("OSF_")
+    assert osf.osf_status_string(99) == "unknown osf status"
+    assert osf.osf_version() >= 100
+
+
+def test_invalid_arguments_rejected_on_host(osf):
+    lib = osf.lib()
+    p = ctypes.c_void_p(1 << 40)
+    o = ctypes.c_void_p(1 << 44)
+    # negative sizes / bad head dim
+    assert lib.osf_attn_fwd(p, p, p, o, -1, 4, 4, None) == osf.OSF_ERR_INVALID
+    assert lib.osf_attn_fwd(p, p, p, o, 4, 4, 0, None) == osf.OSF_ERR_INVALID
+    # empty problems are a no-op (the pages return early on N == 0)
+    assert lib.osf_attn_fwd(None, None, None, None, 0, 4, 4, None) == osf.OSF_OK
+    assert lib.osf_attn_fwd(None, None, None, None, 4, 0, 4, None) == osf.OSF_OK
+    # Hq not divisible by Hkv, unknown dtype, causal with 1 < Sq != Sk, D too large
+    args = lambda dt, Hq, Hkv, Sq, Sk, D, causal: (p, p, p, o, dt, 1, Hq, Hkv, Sq, Sk, D, causal,
+                                                    0.0, None, None, 0, None)
+    assert lib.osf_attn_fwd_gqa(*args(1, 6, 4, 8, 8, 64, 0)) == osf.OSF_ERR_INVALID
+    assert lib.osf_attn_fwd_gqa(*args(7, 4, 4, 8, 8, 64, 0)) == osf.OSF_ERR_INVALID
+    assert lib.osf_attn_fwd_gqa(*args(1, 4, 4, 8, 9, 64, 1)) == osf.OSF_ERR_INVALID
+    assert lib.osf_attn_fwd_gqa(*args(1, 4, 4, 8, 8, 257, 0)) == osf.OSF_ERR_UNSUPPORTED
+    assert lib.osf_attn_fwd_gqa(*args(1, 4, 4, 0, 8, 64, 0)) == osf.OSF_OK
+    # NULL with non-zero size
+    assert lib.osf_attn_fwd_gqa(None, p, p, o, 1, 1, 4, 4, 8, 8, 64, 0, 0.0, None, None, 0,
+                                None) == osf.OSF_ERR_INVALID
+    # output overlapping an input
+    assert lib.osf_attn_fwd_gqa(p, p, p, p, 1, 1, 4, 4, 8, 8, 64, 0, 0.0, None, None, 0,
+                                None) == osf.OSF_ERR_INVALID
+    # softmax: negative sizes, NULL, partial overlap; z == x is allowed (checked on GPU)
+    assert lib.osf_softmax_rows(p, o, -1, 4, None, 0, None) == osf.OSF_ERR_INVALID
+    assert lib.osf_softmax_rows(None, o, 2, 4, None, 0, None) == osf.OSF_ERR_INVALID
+    assert lib.osf_softmax_rows(p, ctypes.c_void_p((1 << 40) + 4), 2, 4, None, 0, None) == osf.OSF_ERR_INVALID
+    assert lib.osf_softmax_rows(None, None, 0, 4, None, 0, None) == osf.OSF_OK
+    n = ctypes.c_size_t(123)
+    assert lib.osf_softmax_workspace_bytes(-1, 4, ctypes.byref(n)) == osf.OSF_ERR_INVALID
+    assert lib.osf_attn_workspace_bytes(1, 1, 3, 2, 1, 8, 64, ctypes.byref(n)) == osf.OSF_ERR_INVALID
+
+
+def test_binding_refuses_cpu_tensors(osf):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        osf.osf_softmax_rows(x)
+    with pytest.raises(ValueError):
+        osf.osf_attn_fwd(x, x, x, x, 4, 4, 8)
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "online_softmax_flash_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "seeded_inputs" not in src, f
