@@ -132,6 +132,27 @@ int osf_softmax_rows(const float *x, float *z, long long rows, long long T,
 int osf_softmax_workspace_bytes(long long rows, long long T, size_t *bytes);
 
 /*
+ * osf_softmax_rows_noalloc -- osf_softmax_rows for callers that cannot allocate device memory.
+ * The pages have no counterpart: this entry point exists for callers such as code running
+ * while a CUDA graph is captured, a library that is handed only its input and output buffers
+ * by an engine owning every allocation, or a process under a fixed device-memory budget.
+ * Same arguments, result and in-place rule as osf_softmax_rows, minus the workspace: the
+ * chunked path keeps its per-chunk (m, l) states in a fixed device array inside the library
+ * (16384 states, 128 KiB, held on every GPU that loads the library until the process exits).
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device, with that device current, looks up the array's device
+ *     address; make that first call before any stream capture.
+ *   - Every call shares the one array per device: calls that may run at the same time on the
+ *     GPU (different streams, or different host threads) race and must be serialised by the
+ *     caller.  Nothing in the array needs to start at zero; each call overwrites what it reads.
+ *   - A problem needing more states than the array holds (only rows longer than 32768
+ *     elements use any: rows x chunks per row > 16384) returns OSF_ERR_WORKSPACE and launches
+ *     nothing; use osf_softmax_rows with a caller workspace instead.
+ */
+int osf_softmax_rows_noalloc(const float *x, float *z, long long rows, long long T,
+                             osf_stream stream);
+
+/*
  * osf_device_status -- synchronise `stream`, then return (and reset to OSF_OK) the device
  * status word of the current device: OSF_ERR_TIMEOUT if any kernel gave up a bounded wait
  * since the last call, OSF_ERR_CUDA if the synchronisation itself failed, else OSF_OK.
