@@ -130,7 +130,7 @@ Path choose_path(const AttnProblem &p, const void *Q, const void *K, const void 
 }
 
 int plan_splits(const AttnProblem &p, Path path, int sm_count, int requested) {
-    if (path == Path::TensorCore) return 1;
+    if (path == Path::TensorCore) return attn_tc_pick_splits(p, sm_count);
     if (path == Path::Decode) return decode_pick_splits(p, sm_count, requested);
     if (requested > 0) {
         const int n_kt = (p.Sk + 63) / 64;
@@ -142,7 +142,6 @@ int plan_splits(const AttnProblem &p, Path path, int sm_count, int requested) {
 size_t path_workspace(const AttnProblem &p, Path path, int splits) {
     const long long rows = (long long)p.B * p.Hq * p.Sq;
     if (path == Path::Decode) return decode_workspace_bytes(p, splits);
-    if (path == Path::TensorCore) return 0;
     return partial_bytes(splits, rows, p.D);
 }
 
@@ -155,6 +154,7 @@ int run_gqa(AttnProblem &p, Path path, void *workspace, size_t workspace_bytes, 
     const long long rows = (long long)p.B * p.Hq * p.Sq;
     switch (path) {
         case Path::TensorCore:
+            if (splits > 1) carve_partials(p, workspace, rows);
             return launch_status(launch_attn_tc(p, dev->sm_count, s));
         case Path::Decode:
             return launch_status(launch_decode(p, workspace, dev->sm_count, s));
@@ -225,6 +225,10 @@ int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, 
     if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
     // the larger of the possible paths' needs (alignment decides the path at call time)
     size_t need = partial_bytes(attn_simt_pick_splits(p, dev->sm_count), (long long)B * Hq * Sq, D);
+    if (dtype == OSF_BF16 && Sq > 1 && (D == 64 || D == 128)) {
+        const size_t tc = partial_bytes(attn_tc_pick_splits(p, dev->sm_count), (long long)B * Hq * Sq, D);
+        if (tc > need) need = tc;
+    }
     if (dtype == OSF_BF16 && Sq == 1) {
         const size_t dn = decode_workspace_bytes(p, decode_pick_splits(p, dev->sm_count, 0));
         if (dn > need) need = dn;

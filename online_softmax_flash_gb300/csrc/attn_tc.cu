@@ -1,8 +1,479 @@
+// Tensor-core attention prefill for bfloat16 Q/K/V on sm_103a: tcgen05 MMAs with fp32
+// accumulators in tensor memory (TMEM), K/V tiles streamed by TMA into a shared-memory ring,
+// and the online-softmax recurrence run by threads that each own one query row.
+//
+// The method is the single-pass attention of "softmax_attention" (blog.euler0525.cn/posts/
+// 3fb3592b), section "实现思路": per query row a running max, a rescale factor, a running
+// denominator and numerator, keys past the sequence end scored -inf; with the GQA mapping and
+// top-left causal mask of "从零开始写Qwen3（五-其一）使用Triton实现自注意力", sections "自注意力原理"
+// and "GQA".  The page runs one program per query on CUDA cores; here one CTA owns 2 x 128
+// query rows and both matrix products run on the tensor cores:
+//
+//   warp 0      TMA producer: Q tiles once, then K_j / V_j into a KV_STAGES-deep ring
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T (SS), O_t += P_t V_j (A = P from TMEM)
+//   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread r owns TMEM lane r, i.e.
+//               query row r of its tile, so row max and row sum need no cross-thread traffic.
+//
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).  P_t (bf16,
+// two per column) overwrites the first 64 columns of S_t and is read from there by the PV MMA.
+// The two Q tiles are ping-ponged so one tile's softmax overlaps the other tile's MMAs.
+//
+// Scores are kept in base 2 (scale * log2 e folded into one multiplier).  The rescale of O is
+// lazy: a row keeps its reference maximum until a tile raises the maximum by more than 8
+// (a factor 256), so O is rarely touched; the result O / l is the same for any reference.
+//
+// Every mbarrier wait is bounded (2 s); on expiry the CTA records OSF_ERR_TIMEOUT in the
+// device status word, drains its own MMAs and copies, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "attn_tc.cuh"
+#include "sm100_ptx.cuh"
 
 namespace osf {
-bool attn_tc_supported(const AttnProblem &, const void *, const void *, const void *, const void *) {
-    return false;
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;             // query rows per Q tile
+constexpr int BN = 128;             // keys per K/V tile
+constexpr int NTHREADS = 384;       // 12 warps: 0-3 control, 4-7 softmax tile 0, 8-11 tile 1
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float kRescaleThreshold = 8.0f;   // base-2 units
+constexpr uint32_t BOX_BYTES = 128 * 128;   // one [128 rows x 64 bf16] box (128-byte rows)
+
+template <int D>
+struct TcCfg {
+    static constexpr int BOXES = D / 64;
+    static constexpr int KV_STAGES = D == 64 ? 4 : 2;
+    static constexpr uint32_t TILE_BYTES = BOXES * BOX_BYTES;        // [128 x D] bf16
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t K_OFF = 2 * TILE_BYTES;
+    static constexpr uint32_t V_OFF = K_OFF + KV_STAGES * TILE_BYTES;
+    static constexpr uint32_t SMEM_BYTES = V_OFF + KV_STAGES * TILE_BYTES + 1024;  // + alignment slack
+    static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
+};
+
+struct Barriers {
+    uint64_t q;
+    uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+    uint64_t s_full[2], p_full[2], o_final[2];
+    uint64_t drain;
+};
+
+__device__ __forceinline__ void raise_timeout(volatile int *abort, int *status) {
+    *abort = 1;
+    if (status) atomicExch(status, kStatusTimeout);
 }
-cudaError_t launch_attn_tc(const AttnProblem &, int, cudaStream_t) { return cudaErrorNotSupported; }
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const AttnProblem p, int n_qb) {
+    using C = TcCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ Barriers bars;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = sbase + C::Q_OFF, sK = sbase + C::K_OFF, sV = sbase + C::V_OFF;
+
+    // ------------------------------------------------------------------ work item
+    const int BH = p.B * p.Hq;
+    const int qb_rank = blockIdx.x / BH;
+    const int bh = blockIdx.x % BH;
+    const int qb = p.causal ? (n_qb - 1 - qb_rank) : qb_rank;   // heaviest blocks first
+    const int q0 = qb * 2 * BM;
+    const int b = bh / p.Hq, hq = bh % p.Hq;
+    const int kvbh = b * p.Hkv + hq / (p.Hq / p.Hkv);
+    const int ntiles = (q0 + BM < p.Sq) ? 2 : 1;
+    const int n_kt_all = (p.Sk + BN - 1) / BN;
+    const int tps = (n_kt_all + p.splits - 1) / p.splits;
+    const int kt_begin = blockIdx.y * tps;
+    const int kt_end = min(n_kt_all, kt_begin + tps);
+    // key tiles each Q tile visits (causal: up to its last row; Q tile 1 may be absent)
+    int e0 = kt_end, e1 = kt_end;
+    if (p.causal) {
+        e0 = min(e0, min(q0 + BM - 1, p.Sq - 1) / BN + 1);
+        e1 = min(e1, min(q0 + 2 * BM - 1, p.Sq - 1) / BN + 1);
+    }
+    const int n0 = max(0, e0 - kt_begin);
+    const int n1 = ntiles == 2 ? max(0, e1 - kt_begin) : 0;
+    const int n_kv = max(n0, n1);
+
+    // ------------------------------------------------------------------ set-up
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
+    if (tid == 32) {
+        mbar_init(smem_u32(&bars.q), 1);
+        for (int s = 0; s < C::KV_STAGES; ++s) {
+            mbar_init(smem_u32(&bars.k_full[s]), 1);
+            mbar_init(smem_u32(&bars.k_empty[s]), 1);
+            mbar_init(smem_u32(&bars.v_full[s]), 1);
+            mbar_init(smem_u32(&bars.v_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bars.s_full[t]), 1);
+            mbar_init(smem_u32(&bars.p_full[t]), BM);
+            mbar_init(smem_u32(&bars.o_final[t]), 1);
+        }
+        mbar_init(smem_u32(&bars.drain), 1);
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0 && lane == 0 && n_kv > 0) {
+        // ============================================================== TMA producer
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+        const uint32_t bq = smem_u32(&bars.q);
+        mbar_expect_tx(bq, ntiles * C::TILE_BYTES);
+        for (int t = 0; t < ntiles; ++t)
+            for (int x = 0; x < C::BOXES; ++x)
+                tma_load_3d(sQ + t * C::TILE_BYTES + x * BOX_BYTES, &mq, bq, x * 64, q0 + t * BM, bh);
+        int issued = 0;
+        bool ok = true;
+        for (int i = 0; i < n_kv && ok; ++i) {
+            const int st = i % C::KV_STAGES;
+            const uint32_t ph = (i / C::KV_STAGES) & 1;
+            const int key0 = (kt_begin + i) * BN;
+            ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, &abort_flag);
+            if (!ok) break;
+            mbar_expect_tx(smem_u32(&bars.k_full[st]), C::TILE_BYTES);
+            for (int x = 0; x < C::BOXES; ++x)
+                tma_load_3d(sK + st * C::TILE_BYTES + x * BOX_BYTES, &mk, smem_u32(&bars.k_full[st]), x * 64, key0,
+                            kvbh);
+            ok = mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, &abort_flag);
+            if (!ok) { issued = 2 * i + 1; break; }
+            mbar_expect_tx(smem_u32(&bars.v_full[st]), C::TILE_BYTES);
+            for (int x = 0; x < C::BOXES; ++x)
+                tma_load_3d(sV + st * C::TILE_BYTES + x * BOX_BYTES, &mv, smem_u32(&bars.v_full[st]), x * 64, key0,
+                            kvbh);
+            issued = 2 * i + 2;
+        }
+        if (!ok) {
+            raise_timeout(&abort_flag, p.status);
+            // let the copies already issued land before the CTA's shared memory is released
+            volatile int no_abort = 0;
+            mbar_wait(bq, 0, &no_abort, 20000000ull);
+            const int nk = (issued + 1) / 2, nv = issued / 2;
+            for (int i = max(0, nk - C::KV_STAGES); i < nk; ++i)
+                mbar_wait(smem_u32(&bars.k_full[i % C::KV_STAGES]), (i / C::KV_STAGES) & 1, &no_abort, 20000000ull);
+            for (int i = max(0, nv - C::KV_STAGES); i < nv; ++i)
+                mbar_wait(smem_u32(&bars.v_full[i % C::KV_STAGES]), (i / C::KV_STAGES) & 1, &no_abort, 20000000ull);
+        }
+    } else if (warp == 1 && lane == 0 && n_kv > 0) {
+        // ============================================================== MMA issuer
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
+        auto issue_s = [&](int t, int st) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * BOX_BYTES + (k & 3) * 32;
+                mma_ss(tmem + (t ? C::S_COL1 : C::S_COL0), sdesc_sw128(sQ + t * C::TILE_BYTES + off, 16, 1024),
+                       sdesc_sw128(sK + st * C::TILE_BYTES + off, 16, 1024), idesc_qk, k > 0);
+            }
+        };
+        auto issue_pv = [&](int t, int st, bool acc) {
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+                mma_ts(tmem + (t ? C::O_COL1 : C::O_COL0), tmem + (t ? C::S_COL1 : C::S_COL0) + k * 8,
+                       sdesc_sw128(sV + st * C::TILE_BYTES + k * 2048, BOX_BYTES, 1024), idesc_pv, acc || k > 0);
+        };
+        bool ok = mbar_wait(smem_u32(&bars.q), 0, &abort_flag);
+        if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, &abort_flag);
+        if (ok) {
+            tc_fence_after();
+            if (n0 > 0) {
+                issue_s(0, 0);
+                mma_commit(smem_u32(&bars.s_full[0]));
+            }
+            if (n1 > 0) {
+                issue_s(1, 0);
+                mma_commit(smem_u32(&bars.s_full[1]));
+            }
+            mma_commit(smem_u32(&bars.k_empty[0]));
+        }
+        for (int i = 0; i < n_kv && ok; ++i) {
+            const int st = i % C::KV_STAGES;
+            const int nx = i + 1;
+            const int st2 = nx % C::KV_STAGES;
+            ok = mbar_wait(smem_u32(&bars.v_full[st]), (i / C::KV_STAGES) & 1, &abort_flag);
+            if (!ok) break;
+            if (i < n0) {
+                ok = mbar_wait(smem_u32(&bars.p_full[0]), i & 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, st, i > 0);
+                if (i == n0 - 1) mma_commit(smem_u32(&bars.o_final[0]));
+            }
+            if (nx < n_kv) {
+                ok = mbar_wait(smem_u32(&bars.k_full[st2]), (nx / C::KV_STAGES) & 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                if (nx < n0) {
+                    issue_s(0, st2);
+                    mma_commit(smem_u32(&bars.s_full[0]));
+                }
+            }
+            if (i < n1) {
+                ok = mbar_wait(smem_u32(&bars.p_full[1]), i & 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(1, st, i > 0);
+                if (i == n1 - 1) mma_commit(smem_u32(&bars.o_final[1]));
+            }
+            mma_commit(smem_u32(&bars.v_empty[st]));
+            if (nx < n_kv) {
+                if (nx < n1) {
+                    issue_s(1, st2);
+                    mma_commit(smem_u32(&bars.s_full[1]));
+                }
+                mma_commit(smem_u32(&bars.k_empty[st2]));
+            }
+        }
+        if (!ok) raise_timeout(&abort_flag, p.status);
+        // every MMA issued above completes before TMEM is released
+        mma_commit(smem_u32(&bars.drain));
+        volatile int no_abort = 0;
+        mbar_wait(smem_u32(&bars.drain), 0, &no_abort, 20000000ull);
+    } else if (warp >= 4) {
+        // ============================================================== softmax
+        const int t = (warp - 4) >> 2;           // Q tile
+        const int r = tid - 128 * (t + 1);       // row within the tile == TMEM lane
+        const int row = q0 + t * BM + r;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t s_addr = lane_base + (t ? C::S_COL1 : C::S_COL0);
+        const uint32_t o_addr = lane_base + (t ? C::O_COL1 : C::O_COL0);
+        const int nt = t ? n1 : n0;
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int i = 0; i < nt; ++i) {
+            ok = mbar_wait(smem_u32(&bars.s_full[t]), i & 1, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+            tmem_ld_wait();
+            const int key0 = (kt_begin + i) * BN;
+            const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > q0 + t * BM);
+            float mx = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int key = key0 + c * 32 + k;
+                        const bool valid = key < p.Sk && (!p.causal || key <= row);
+                        float v = valid ? __uint_as_float(sr[c][k]) : -INFINITY;
+                        sr[c][k] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(sr[c][k]));
+            }
+            const float m_tile = mx * sl2;   // -inf stays -inf (sl2 > 0)
+            const float m_new = fmaxf(m_ref, m_tile);
+            const bool rescale = __any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold);
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = ex2_approx(m_ref - m_new);   // m_ref == -inf -> 0
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * k]), sl2, -mr));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * k + 1]), sl2, -mr));
+                    rs += p0 + p1;
+                    sr[c][k] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
+                          sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
+                          sr[c][15]);
+            }
+            if (rescale && i > 0) {
+                // O_t += P V of earlier tiles has completed: the commit that signalled s_full
+                // for this tile covers every MMA issued before it.  The PV MMA of this tile
+                // waits for p_full, signalled below, after the rescaled O is stored.
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st32(o_addr + c * 32, o);
+                }
+            }
+            l += rs;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_full[t]));
+        }
+        if (!ok) raise_timeout(&abort_flag, p.status);
+        // ---------------------------------------------------------- epilogue
+        if (t < ntiles) {
+            bool have_o = false;
+            if (ok && nt > 0) {
+                ok = mbar_wait(smem_u32(&bars.o_final[t]), 0, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) raise_timeout(&abort_flag, p.status);
+                have_o = ok;
+                tc_fence_after();
+            }
+            const long long rows_total = (long long)p.B * p.Hq * p.Sq;
+            const long long grow = (long long)bh * p.Sq + row;
+            const bool row_ok = row < p.Sq;
+            if (p.splits == 1) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + grow * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    if (have_o) {
+                        tmem_ld32(o_addr + c * 32, o);
+                        tmem_ld_wait();
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        pk[k] = have_o ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv)
+                                       : 0u;
+                    if (row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(Og + c * 32);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
+                }
+                if (p.lse && row_ok) p.lse[grow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+            } else {
+                float *A = p.part_acc + ((size_t)blockIdx.y * rows_total + grow) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    if (have_o) {
+                        tmem_ld32(o_addr + c * 32, o);
+                        tmem_ld_wait();
+                    }
+                    if (row_ok) {
+                        float4 *dst = reinterpret_cast<float4 *>(A + c * 32);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = have_o ? make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                          __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                if (row_ok) {
+                    p.part_m[(size_t)blockIdx.y * rows_total + grow] = have_o ? m_ref : -INFINITY;
+                    p.part_l[(size_t)blockIdx.y * rows_total + grow] = have_o ? l : 0.f;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D map over a contiguous [Z][Y][D] bf16 tensor; box [1][128][64]; 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *g, int D, long long Y, long long Z) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Y, (cuuint64_t)Z};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)Y};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(g), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int D>
+cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
+    using C = TcCfg<D>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)C::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, p.q, D, p.Sq, (long long)p.B * p.Hq) || !make_map(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv) ||
+        !make_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv))
+        return cudaErrorInvalidValue;
+    const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
+    dim3 grid((unsigned)(n_qb * p.B * p.Hq), (unsigned)p.splits);
+    attn_tc_kernel<D><<<grid, NTHREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p, n_qb);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(const AttnProblem &p, const void *Q, const void *K, const void *V, const void *O) {
+    if (p.dtype != OSF_BF16 || p.Sq < 2 || (p.D != 64 && p.D != 128)) return false;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return false;
+    if ((long long)p.B * p.Hq * ((p.Sq + 2 * BM - 1) / (2 * BM)) >= (1LL << 31)) return false;
+    return encode_fn() != nullptr;
+}
+
+int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {
+    const long long ctas = (long long)((p.Sq + 2 * BM - 1) / (2 * BM)) * p.B * p.Hq;
+    const int n_kt = (p.Sk + BN - 1) / BN;
+    if (ctas >= sm_count || n_kt <= 1) return 1;
+    int want = (int)((sm_count + ctas - 1) / ctas);
+    if (want > n_kt) want = n_kt;
+    const int tps = (n_kt + want - 1) / want;
+    return (n_kt + tps - 1) / tps;   // no empty split
+}
+
+cudaError_t launch_attn_tc(const AttnProblem &p, int sm_count, cudaStream_t s) {
+    (void)sm_count;
+    cudaError_t e = p.D == 64 ? launch_t<64>(p, s) : launch_t<128>(p, s);
+    if (e == cudaSuccess && p.splits > 1) e = launch_attn_combine(p, s);
+    return e;
+}
+
 }  // namespace osf
