@@ -140,9 +140,8 @@ int plan_splits(const AttnProblem &p, Path path, int sm_count, int requested) {
 }
 
 size_t path_workspace(const AttnProblem &p, Path path, int splits) {
-    const long long rows = (long long)p.B * p.Hq * p.Sq;
-    if (path == Path::Decode) return decode_workspace_bytes(p, splits);
-    return partial_bytes(splits, rows, p.D);
+    (void)path;  // every path keeps split partial states in the same layout
+    return partial_bytes(splits, (long long)p.B * p.Hq * p.Sq, p.D);
 }
 
 int run_gqa(AttnProblem &p, Path path, void *workspace, size_t workspace_bytes, int splits,
@@ -157,7 +156,8 @@ int run_gqa(AttnProblem &p, Path path, void *workspace, size_t workspace_bytes, 
             if (splits > 1) carve_partials(p, workspace, rows);
             return launch_status(launch_attn_tc(p, dev->sm_count, s));
         case Path::Decode:
-            return launch_status(launch_decode(p, workspace, dev->sm_count, s));
+            if (splits > 1) carve_partials(p, workspace, rows);
+            return launch_status(launch_decode(p, s));
         case Path::Simt:
         default: {
             if (splits > 1) carve_partials(p, workspace, rows);
@@ -230,7 +230,7 @@ int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, 
         if (tc > need) need = tc;
     }
     if (dtype == OSF_BF16 && Sq == 1) {
-        const size_t dn = decode_workspace_bytes(p, decode_pick_splits(p, dev->sm_count, 0));
+        const size_t dn = partial_bytes(decode_pick_splits(p, dev->sm_count, 0), (long long)B * Hq, D);
         if (dn > need) need = dn;
     }
     *bytes = need;
@@ -265,7 +265,7 @@ int osf_attn_decode_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sk, i
     if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
     size_t need = partial_bytes(plan_splits(p, Path::Simt, dev->sm_count, num_splits), (long long)B * Hq, D);
     if (dtype == OSF_BF16) {
-        const size_t dn = decode_workspace_bytes(p, decode_pick_splits(p, dev->sm_count, num_splits));
+        const size_t dn = partial_bytes(decode_pick_splits(p, dev->sm_count, num_splits), (long long)B * Hq, D);
         if (dn > need) need = dn;
     }
     *bytes = need;

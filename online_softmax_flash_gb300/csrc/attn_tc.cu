@@ -24,12 +24,11 @@
 //
 // Every mbarrier wait is bounded (2 s); on expiry the CTA records OSF_ERR_TIMEOUT in the
 // device status word, drains its own MMAs and copies, frees TMEM and exits.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "attn_tc.cuh"
 #include "sm100_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace osf {
 namespace {
@@ -392,6 +391,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     }
 
     tc_fence_before();
+    __syncwarp();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
@@ -400,35 +400,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 }
 
 // ------------------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// 3-D map over a contiguous [Z][Y][D] bf16 tensor; box [1][128][64]; 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *g, int D, long long Y, long long Z) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Y, (cuuint64_t)Z};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)Y};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(g), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 template <int D>
 cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     using C = TcCfg<D>;
@@ -440,8 +411,9 @@ cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, D, p.Sq, (long long)p.B * p.Hq) || !make_map(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv) ||
-        !make_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv))
+    if (!make_bf16_map_3d(&mq, p.q, D, p.Sq, (long long)p.B * p.Hq, 128) ||
+        !make_bf16_map_3d(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, 128) ||
+        !make_bf16_map_3d(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, 128))
         return cudaErrorInvalidValue;
     const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
     dim3 grid((unsigned)(n_qb * p.B * p.Hq), (unsigned)p.splits);
@@ -456,7 +428,7 @@ bool attn_tc_supported(const AttnProblem &p, const void *Q, const void *K, const
     if (p.dtype != OSF_BF16 || p.Sq < 2 || (p.D != 64 && p.D != 128)) return false;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return false;
     if ((long long)p.B * p.Hq * ((p.Sq + 2 * BM - 1) / (2 * BM)) >= (1LL << 31)) return false;
-    return encode_fn() != nullptr;
+    return tensor_map_encoder() != nullptr;
 }
 
 int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {
