@@ -8,7 +8,9 @@ d=32 single head, split-K decode, row softmax, 1-D softmax) are measured after i
 run and reported under "suite".
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA events on the
-launching stream; L2 is flushed (a 512 MiB write) between timed steps, outside the events.
+launching stream; between timed steps, outside the events, L2 is flushed by writing a 512 MiB
+buffer and then reading a second 256 MiB one (so no dirty lines are left behind to be written back
+during the next step).
 Barrier + synchronize on both sides of the timed loop; the max over ranks is reported.
 With torchrun (N > 1) every rank runs its own replica of the workload (weak scaling: the
 path shards over (batch, kv head) with no exchange).
@@ -176,7 +178,7 @@ class Runner:
 
 # ------------------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (100 ms) kept only while the timed region is open."""
+    """nvidia-smi samples (every 50 ms) kept while the measured loop (warm-up + timed steps) runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -196,7 +198,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -224,13 +226,30 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for s in self.samples for n, v in zip(names, s[5:9]) if v.strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(self.samples), "window": "warm-up + timed steps"}
 
 
 # ----------------------------------------------------------------------------- timing
+def make_flush(dev):
+    import torch
+    return (torch.empty(128 << 20, dtype=torch.float32, device=dev),   # 512 MiB, written
+            torch.ones(64 << 20, dtype=torch.float32, device=dev),     # 256 MiB, read
+            torch.empty(1, dtype=torch.float32, device=dev))
+
+
+def flush_l2(flush):
+    """Evict L2 (129 MB on GB300): write a buffer larger than L2, then read another one."""
+    import torch
+    w, r, sink = flush
+    w.fill_(1.0)
+    torch.sum(r, dim=0, out=sink[0])
+
+
 def time_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
     """Per-step CUDA-event times (ms) of ``fn`` on ``stream``, L2 flushed between steps."""
     import torch
+    if sampler:
+        sampler.open = True
     for _ in range(warmup):
         fn()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -239,12 +258,10 @@ def time_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
     if barrier:
         barrier()
     torch.cuda.synchronize()
-    if sampler:
-        sampler.open = True
     t0 = time.perf_counter()
     for i in range(steps):
         if flush is not None:
-            flush.add_(1)
+            flush_l2(flush)
         starts[i].record(stream)
         fn()
         ends[i].record(stream)
@@ -428,7 +445,7 @@ def main():
     torch.cuda.set_device(dev)
     osf.lib()
     pk, pk_src = peaks()
-    flush = torch.empty(128 << 20, dtype=torch.float32, device=dev)  # 512 MiB > L2
+    flush = make_flush(dev)
 
     w = WORKLOADS[args.workload]
     sampler = ClockSampler(local)
@@ -471,7 +488,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.get("dtype", "f32"), "data": "synthetic",
-            "config": {"workload": w["desc"], "l2": "flushed (512 MiB write) between timed steps",
+            "config": {"workload": w["desc"], "l2": "flushed between timed steps (512 MiB write, then 256 MiB read)",
                        "inputs": "seeded i.i.d. N(0,1) (SplitMix64 + Box-Muller), resident in HBM",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": rl, "cpu_baseline": cpu,

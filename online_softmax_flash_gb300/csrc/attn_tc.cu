@@ -9,7 +9,7 @@
 // and "GQA".  The page runs one program per query on CUDA cores; here one CTA owns 2 x 128
 // query rows and both matrix products run on the tensor cores:
 //
-//   warp 0      TMA producer: Q tiles once, then K_j / V_j into a KV_STAGES-deep ring
+//   warps 0, 2  TMA producers: Q tiles once and K_j (warp 0), V_j (warp 2), KV_STAGES-deep rings
 //   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T (SS), O_t += P_t V_j (A = P from TMEM)
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread r owns TMEM lane r, i.e.
 //               query row r of its tile, so row max and row sum need no cross-thread traffic.
@@ -39,6 +39,10 @@ constexpr int BM = 128;             // query rows per Q tile
 constexpr int BN = 128;             // keys per K/V tile
 constexpr int NTHREADS = 384;       // 12 warps: 0-3 control, 4-7 softmax tile 0, 8-11 tile 1
 constexpr uint32_t TMEM_COLS = 512;
+// Register split after set-up: the control warpgroup (TMA + MMA issue) needs few registers, the
+// two softmax warpgroups hold a whole 128-column score row each.  128*56 + 256*224 = 384*168,
+// the registers the CTA is launched with (168 per thread).
+constexpr int kCtrlRegs = 56, kSoftmaxRegs = 224;
 constexpr float kRescaleThreshold = 8.0f;   // base-2 units
 constexpr uint32_t BOX_BYTES = 128 * 128;   // one [128 rows x 64 bf16] box (128-byte rows)
 
@@ -128,64 +132,64 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 0 && lane == 0 && n_kv > 0) {
-        // ============================================================== TMA producer
-        tma_prefetch_desc(&mq);
-        tma_prefetch_desc(&mk);
-        tma_prefetch_desc(&mv);
+    if (warp < 4) {
+      setmaxnreg_dec<kCtrlRegs>();
+      if ((warp == 0 || warp == 2) && lane == 0 && n_kv > 0) {
+        // ============================================================== TMA producers
+        // warp 0 streams Q and K, warp 2 streams V: each tile is one TMA instruction, and the
+        // two streams are issued by different threads so neither waits behind the other.
+        const bool is_k = warp == 0;
+        const CUtensorMap *map = is_k ? &mk : &mv;
+        tma_prefetch_desc(map);
         const uint32_t bq = smem_u32(&bars.q);
-        mbar_expect_tx(bq, ntiles * C::TILE_BYTES);
-        for (int t = 0; t < ntiles; ++t)
-            for (int x = 0; x < C::BOXES; ++x)
-                tma_load_3d(sQ + t * C::TILE_BYTES + x * BOX_BYTES, &mq, bq, x * 64, q0 + t * BM, bh);
+        if (is_k) {
+            tma_prefetch_desc(&mq);
+            mbar_expect_tx(bq, ntiles * C::TILE_BYTES);
+            for (int t = 0; t < ntiles; ++t) tma_load_tile(sQ + t * C::TILE_BYTES, &mq, bq, q0 + t * BM, bh);
+        }
+        const uint32_t ring = is_k ? sK : sV;
+        uint64_t *full = is_k ? bars.k_full : bars.v_full;
+        uint64_t *empty = is_k ? bars.k_empty : bars.v_empty;
         int issued = 0;
         bool ok = true;
-        for (int i = 0; i < n_kv && ok; ++i) {
+        for (int i = 0; i < n_kv; ++i) {
             const int st = i % C::KV_STAGES;
-            const uint32_t ph = (i / C::KV_STAGES) & 1;
-            const int key0 = (kt_begin + i) * BN;
-            ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, &abort_flag);
+            ok = mbar_wait(smem_u32(&empty[st]), ((i / C::KV_STAGES) & 1) ^ 1, &abort_flag);
             if (!ok) break;
-            mbar_expect_tx(smem_u32(&bars.k_full[st]), C::TILE_BYTES);
-            for (int x = 0; x < C::BOXES; ++x)
-                tma_load_3d(sK + st * C::TILE_BYTES + x * BOX_BYTES, &mk, smem_u32(&bars.k_full[st]), x * 64, key0,
-                            kvbh);
-            ok = mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, &abort_flag);
-            if (!ok) { issued = 2 * i + 1; break; }
-            mbar_expect_tx(smem_u32(&bars.v_full[st]), C::TILE_BYTES);
-            for (int x = 0; x < C::BOXES; ++x)
-                tma_load_3d(sV + st * C::TILE_BYTES + x * BOX_BYTES, &mv, smem_u32(&bars.v_full[st]), x * 64, key0,
-                            kvbh);
-            issued = 2 * i + 2;
+            mbar_expect_tx(smem_u32(&full[st]), C::TILE_BYTES);
+            tma_load_tile(ring + st * C::TILE_BYTES, map, smem_u32(&full[st]), (kt_begin + i) * BN, kvbh);
+            issued = i + 1;
         }
         if (!ok) {
             raise_timeout(&abort_flag, p.status);
             // let the copies already issued land before the CTA's shared memory is released
-            volatile int no_abort = 0;
-            mbar_wait(bq, 0, &no_abort, 20000000ull);
-            const int nk = (issued + 1) / 2, nv = issued / 2;
-            for (int i = max(0, nk - C::KV_STAGES); i < nk; ++i)
-                mbar_wait(smem_u32(&bars.k_full[i % C::KV_STAGES]), (i / C::KV_STAGES) & 1, &no_abort, 20000000ull);
-            for (int i = max(0, nv - C::KV_STAGES); i < nv; ++i)
-                mbar_wait(smem_u32(&bars.v_full[i % C::KV_STAGES]), (i / C::KV_STAGES) & 1, &no_abort, 20000000ull);
+            if (is_k) mbar_wait(bq, 0, nullptr, 20000000ull);
+            for (int i = max(0, issued - C::KV_STAGES); i < issued; ++i)
+                mbar_wait(smem_u32(&full[i % C::KV_STAGES]), (i / C::KV_STAGES) & 1, nullptr, 20000000ull);
         }
-    } else if (warp == 1 && lane == 0 && n_kv > 0) {
+      } else if (warp == 1 && lane == 0 && n_kv > 0) {
         // ============================================================== MMA issuer
         constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
+        // Descriptors are built once per operand tile; stepping along K adds the byte offset
+        // (>> 4) to the start-address field, which cannot carry out of its 14 bits because
+        // shared-memory addresses stay below 256 KiB.
         auto issue_s = [&](int t, int st) {
+            const uint64_t qd = sdesc_sw128(sQ + t * C::TILE_BYTES, 16, 1024);
+            const uint64_t kd = sdesc_sw128(sK + st * C::TILE_BYTES, 16, 1024);
+            const uint32_t dst = tmem + (t ? C::S_COL1 : C::S_COL0);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * BOX_BYTES + (k & 3) * 32;
-                mma_ss(tmem + (t ? C::S_COL1 : C::S_COL0), sdesc_sw128(sQ + t * C::TILE_BYTES + off, 16, 1024),
-                       sdesc_sw128(sK + st * C::TILE_BYTES + off, 16, 1024), idesc_qk, k > 0);
+                const uint32_t off = ((k >> 2) * BOX_BYTES + (k & 3) * 32) >> 4;
+                mma_ss(dst, qd + off, kd + off, idesc_qk, k > 0);
             }
         };
         auto issue_pv = [&](int t, int st, bool acc) {
+            const uint64_t vd = sdesc_sw128(sV + st * C::TILE_BYTES, BOX_BYTES, 1024);
+            const uint32_t dst = tmem + (t ? C::O_COL1 : C::O_COL0);
+            const uint32_t pa = tmem + (t ? C::S_COL1 : C::S_COL0);
 #pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-                mma_ts(tmem + (t ? C::O_COL1 : C::O_COL0), tmem + (t ? C::S_COL1 : C::S_COL0) + k * 8,
-                       sdesc_sw128(sV + st * C::TILE_BYTES + k * 2048, BOX_BYTES, 1024), idesc_pv, acc || k > 0);
+            for (int k = 0; k < BN / 16; ++k) mma_ts(dst, pa + k * 8, vd + ((k * 2048) >> 4), idesc_pv, acc || k > 0);
         };
         bool ok = mbar_wait(smem_u32(&bars.q), 0, &abort_flag);
         if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, &abort_flag);
@@ -242,9 +246,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         if (!ok) raise_timeout(&abort_flag, p.status);
         // every MMA issued above completes before TMEM is released
         mma_commit(smem_u32(&bars.drain));
-        volatile int no_abort = 0;
-        mbar_wait(smem_u32(&bars.drain), 0, &no_abort, 20000000ull);
-    } else if (warp >= 4) {
+        mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
+      }
+    } else {
+        setmaxnreg_inc<kSoftmaxRegs>();
         // ============================================================== softmax
         const int t = (warp - 4) >> 2;           // Q tile
         const int r = tid - 128 * (t + 1);       // row within the tile == TMEM lane
@@ -267,7 +272,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             tmem_ld_wait();
             const int key0 = (kt_begin + i) * BN;
             const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > q0 + t * BM);
-            float mx = -INFINITY;
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -275,16 +279,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     for (int k = 0; k < 32; ++k) {
                         const int key = key0 + c * 32 + k;
                         const bool valid = key < p.Sk && (!p.causal || key <= row);
-                        float v = valid ? __uint_as_float(sr[c][k]) : -INFINITY;
-                        sr[c][k] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
+                        if (!valid) sr[c][k] = __float_as_uint(-INFINITY);
                     }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(sr[c][k]));
             }
+            // row max: eight independent chains of 3-input max, then a short tree
+            float mm[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const int c = g >> 1, k0 = (g & 1) * 16;
+                mm[g] = fmaxf(__uint_as_float(sr[c][k0]), __uint_as_float(sr[c][k0 + 1]));
+#pragma unroll
+                for (int u = 1; u < 8; ++u)
+                    mm[g] = fmax3(mm[g], __uint_as_float(sr[c][k0 + 2 * u]), __uint_as_float(sr[c][k0 + 2 * u + 1]));
+            }
+            const float mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[7]));
             const float m_tile = mx * sl2;   // -inf stays -inf (sl2 > 0)
             const float m_new = fmaxf(m_ref, m_tile);
             const bool rescale = __any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold);
@@ -295,31 +303,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 m_ref = m_new;
             }
             const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs = 0.f;
+            // p = 2^(s * scale * log2e - m): pairs through one f32x2 FMA, sums in four
+            // independent f32x2 accumulators; P packed to bf16 over the first half of S.
+            const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mr, -mr);
+            uint64_t acc[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                acc[c] = f2_pack(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * k]), sl2, -mr));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * k + 1]), sl2, -mr));
-                    rs += p0 + p1;
+                    float p0, p1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * k]), __uint_as_float(sr[c][2 * k + 1])), sc2, nm2),
+                              p0, p1);
+                    p0 = ex2_approx(p0);
+                    p1 = ex2_approx(p1);
+                    acc[c] = f2_add(acc[c], f2_pack(p0, p1));
                     sr[c][k] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
                           sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
                           sr[c][15]);
             }
+            float rs;
+            {
+                const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+                float lo, hi;
+                f2_unpack(a2, lo, hi);
+                rs = lo + hi;
+            }
             if (rescale && i > 0) {
                 // O_t += P V of earlier tiles has completed: the commit that signalled s_full
                 // for this tile covers every MMA issued before it.  The PV MMA of this tile
                 // waits for p_full, signalled below, after the rescaled O is stored.
+                const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32(o_addr + c * 32, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    for (int k = 0; k < 16; ++k) {
+                        float a, b;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2), a, b);
+                        o[2 * k] = __float_as_uint(a);
+                        o[2 * k + 1] = __float_as_uint(b);
+                    }
                     tmem_st32(o_addr + c * 32, o);
                 }
             }
@@ -411,9 +439,9 @@ cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap mq, mk, mv;
-    if (!make_bf16_map_3d(&mq, p.q, D, p.Sq, (long long)p.B * p.Hq, 128) ||
-        !make_bf16_map_3d(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, 128) ||
-        !make_bf16_map_3d(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, 128))
+    if (!make_bf16_tile_map(&mq, p.q, D, p.Sq, (long long)p.B * p.Hq, BM) ||
+        !make_bf16_tile_map(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, BN) ||
+        !make_bf16_tile_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, BN))
         return cudaErrorInvalidValue;
     const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
     dim3 grid((unsigned)(n_qb * p.B * p.Hq), (unsigned)p.splits);

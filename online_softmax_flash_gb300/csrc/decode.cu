@@ -9,8 +9,8 @@
 // boxed recurrence of "Softmax 算子的实现与优化", "Online Softmax", applied to whole partial
 // states.  (The split is not on the pages; it is the plainest way to spread one row over the GPU.)
 //
-// Inside a CTA: one warp drives TMA loads of 64-key K and V tiles (128-byte swizzle, so the
-// ldmatrix reads below are bank-conflict free) into a 3-stage ring; four compute warps each
+// Inside a CTA: two warps drive TMA loads of 64-key K and V tiles (one instruction per tile,
+// 128-byte swizzle, so the ldmatrix reads below are bank-conflict free) into a 3-stage ring; four compute warps each
 // take 16 keys of every tile and run the recurrence of "softmax_attention", "实现思路" with
 // warp-level tensor-core MMAs (m16n8k16, bf16 in, fp32 accumulate): S = Q K^T with the G query
 // rows padded to 16, then the S accumulator fragments are reused in registers as the P operand
@@ -26,7 +26,7 @@ using namespace ptx;
 
 constexpr int KT = 64;                       // keys per tile
 constexpr int NCW = 4;                       // compute warps, 16 keys of each tile apiece
-constexpr int NTHREADS = (NCW + 1) * 32;     // + the TMA producer warp
+constexpr int NTHREADS = (NCW + 2) * 32;     // + two TMA producer warps (K, V)
 constexpr int STAGES = 3;
 constexpr uint32_t BOXB = 64 * 128;          // one [64 keys x 64 bf16] box, 128-byte rows
 constexpr int MAX_G = 16;                    // query heads per kv head (MMA rows)
@@ -74,7 +74,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&full[s]), 2);   // the K and the V producer each arrive once
             mbar_init(smem_u32(&empty[s]), NCW);
         }
         abort_flag = 0;
@@ -82,11 +82,13 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
     }
     __syncthreads();
 
-    if (warp == NCW) {
-        // ================================================================ TMA producer
+    if (warp >= NCW) {
+        // ================================================================ TMA producers
+        // warp NCW streams K, warp NCW + 1 streams V; each 64-key tile is one TMA instruction.
         if (lane == 0 && ntile > 0) {
-            tma_prefetch_desc(&mk);
-            tma_prefetch_desc(&mv);
+            const CUtensorMap *map = warp == NCW ? &mk : &mv;
+            const uint32_t ring = sbase + (warp == NCW ? C::K_OFF : C::V_OFF);
+            tma_prefetch_desc(map);
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < ntile; ++i) {
@@ -94,25 +96,19 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
                 ok = mbar_wait(smem_u32(&empty[st]), ((i / STAGES) & 1) ^ 1, &abort_flag);
                 if (!ok) break;
                 const uint32_t bar = smem_u32(&full[st]);
-                mbar_expect_tx(bar, 2 * C::TILE);
-                const int key0 = (t_begin + i) * KT;
-#pragma unroll
-                for (int x = 0; x < C::BOXES; ++x) {
-                    tma_load_3d(sbase + C::K_OFF + st * C::TILE + x * BOXB, &mk, bar, x * 64, key0, kvbh);
-                    tma_load_3d(sbase + C::V_OFF + st * C::TILE + x * BOXB, &mv, bar, x * 64, key0, kvbh);
-                }
+                mbar_expect_tx(bar, C::TILE);
+                tma_load_tile(ring + st * C::TILE, map, bar, (t_begin + i) * KT, kvbh);
                 issued = i + 1;
             }
             if (!ok) {
                 abort_flag = 1;
                 atomicExch(p.status, kStatusTimeout);
-                volatile int no_abort = 0;   // let issued copies land before the CTA exits
-                for (int i = max(0, issued - STAGES); i < issued; ++i)
-                    mbar_wait(smem_u32(&full[i % STAGES]), (i / STAGES) & 1, &no_abort, 20000000ull);
+                for (int i = max(0, issued - STAGES); i < issued; ++i)   // let issued copies land
+                    mbar_wait(smem_u32(&full[i % STAGES]), (i / STAGES) & 1, nullptr, 20000000ull);
             }
         }
         // Every issued copy is consumed by the compute warps before they reuse the ring, so
-        // the producer warp can leave now.
+        // the producer warps can leave now.
         return;
     }
 
@@ -266,8 +262,8 @@ cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap mk, mv;
-    if (!make_bf16_map_3d(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, KT) ||
-        !make_bf16_map_3d(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, KT))
+    if (!make_bf16_tile_map(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, KT) ||
+        !make_bf16_tile_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, KT))
         return cudaErrorInvalidValue;
     const int n_kt = (p.Sk + KT - 1) / KT;
     const int tps = (n_kt + p.splits - 1) / p.splits;

@@ -39,6 +39,24 @@ inline bool make_bf16_map_3d(CUtensorMap *m, const void *g, int D, long long Y, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D view (d % 64, y, d / 64, z) of a contiguous bf16 tensor [Z][Y][D], D a multiple of 64:
+// one box {64, box_rows, D/64, 1} brings a whole [box_rows x D] tile in a single TMA
+// instruction, laid out in shared memory as D/64 consecutive [box_rows][64] blocks (128-byte
+// rows, 128-byte swizzle) -- the K-major layout the tcgen05 descriptors expect.  A TMA
+// instruction has a fixed cost of several hundred cycles on this part whatever its size, so
+// fewer, larger boxes keep the copy engine ahead of the tensor core.
+inline bool make_bf16_tile_map(CUtensorMap *m, const void *g, int D, long long Y, long long Z, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc || D % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, (cuuint64_t)Y, (cuuint64_t)(D / 64), (cuuint64_t)Z};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)D * 2 * (cuuint64_t)Y};
+    cuuint32_t box[4] = {64, box_rows, (cuuint32_t)(D / 64), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(g), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace osf
