@@ -65,7 +65,18 @@ SM_COUNT_GB300 = 152
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture) of
 # each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
 # source that changed since the capture reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "63748d2e3eb2c825",
+                           "bytes": 134.56e6, "scope": "attn_tc_kernel<128>, one launch"},
+    "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "f0dd5302023a97d4",
+                   "bytes": 1079.81e6, "scope": "decode_kernel<128>, one launch"},
+    "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "1369193089605318",
+                     "bytes": 1020.95e6, "scope": "softmax_rows_onchip_kernel<8>, one launch"},
+    "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "1369193089605318",
+                   "bytes": 760.90e6, "scope": "step: chunk state + chunk normalise kernels"},
+    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_simt.cu", "sha": "ea58427b628cd84b",
+                             "bytes": 3.17e6, "scope": "attn_simt_kernel<float,64,64>, one launch"},
+}
 
 
 def peaks():
@@ -312,11 +323,11 @@ def roofline(res, pk, w):
     else:  # FP32 FMA pipe
         peak, unit = SM_COUNT_GB300 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12, "TFLOP/s"
     t = TRAFFIC.get(res["name"])
-    traffic = None
+    traffic = scope = None
     if t and source_hash(os.path.join(ROOT, t["source"])) == t["sha"]:
-        traffic = t["bytes"]
+        traffic, scope = t["bytes"], t["scope"]
     return {"bound": res["bound"], "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_scope": scope,
             "algorithmic": round(res["amount"] * (1e12 if unit == "TFLOP/s" else 1e9)),
             "per": "flop" if unit == "TFLOP/s" else "byte"}
 
