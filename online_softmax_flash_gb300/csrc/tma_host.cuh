@@ -45,12 +45,16 @@ inline bool make_bf16_map_3d(CUtensorMap *m, const void *g, int D, long long Y, 
 // rows, 128-byte swizzle) -- the K-major layout the tcgen05 descriptors expect.  A TMA
 // instruction has a fixed cost of several hundred cycles on this part whatever its size, so
 // fewer, larger boxes keep the copy engine ahead of the tensor core.
-inline bool make_bf16_tile_map(CUtensorMap *m, const void *g, int D, long long Y, long long Z, uint32_t box_rows) {
+// `box_dblocks` (default all D/64) 64-column blocks per box: a box of one block loads a
+// [box_rows x 64] column slice.
+inline bool make_bf16_tile_map(CUtensorMap *m, const void *g, int D, long long Y, long long Z, uint32_t box_rows,
+                               uint32_t box_dblocks = 0) {
     auto enc = tensor_map_encoder();
     if (!enc || D % 64 != 0) return false;
+    if (box_dblocks == 0) box_dblocks = (uint32_t)(D / 64);
     cuuint64_t dims[4] = {64, (cuuint64_t)Y, (cuuint64_t)(D / 64), (cuuint64_t)Z};
     cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)D * 2 * (cuuint64_t)Y};
-    cuuint32_t box[4] = {64, box_rows, (cuuint32_t)(D / 64), 1};
+    cuuint32_t box[4] = {64, box_rows, box_dblocks, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(g), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
