@@ -43,10 +43,12 @@ constexpr int BN = 128;             // keys per key tile
 constexpr int NTHREADS = 384;       // 12 warps: 0-3 control, 4-7 softmax tile 0, 8-11 tile 1
 constexpr uint32_t TMEM_COLS = 512;
 // Register split after set-up: the two softmax warpgroups hold a whole 128-column score row
-// each; the control warpgroup (TMA + MMA issue) keeps 72 (with fewer, spilled values in the
-// issue loop slow the stream of MMA instructions).  128*72 + 256*216 = 384*168, the
-// registers the CTA is launched with (168 per thread).
-constexpr int kCtrlRegs = 72, kSoftmaxRegs = 216;
+// each; the control warpgroup (TMA + MMA issue) keeps 104.  Issuing one tcgen05.mma costs the
+// issuing thread about 46 cycles against 64 cycles of tensor work, so any spill or recomputation
+// in the issue loop starves the tensor pipe (its queue holds only a few instructions); below
+// about 88 registers that happened.  128*104 + 256*200 = 384*168, the registers the CTA is
+// launched with (168 per thread).
+constexpr int kCtrlRegs = 104, kSoftmaxRegs = 200;
 constexpr float kRescaleThreshold = 8.0f;   // base-2 units
 
 constexpr uint32_t kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KiB)
@@ -294,14 +296,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const int key0 = (kt_begin + i) * BN;
             const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > row_first);
             if (need_mask) {
+                // column j of the tile (key key0 + j) is kept iff j < lim: inside the sequence
+                // and, when causal, not after this row
+                int lim = p.Sk - key0;
+                if (p.causal) lim = min(lim, row - key0 + 1);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int key = key0 + c * 32 + k;
-                        const bool valid = key < p.Sk && (!p.causal || key <= row);
-                        if (!valid) sr[c][k] = __float_as_uint(-INFINITY);
-                    }
+                    for (int k = 0; k < 32; ++k)
+                        if (c * 32 + k >= lim) sr[c][k] = __float_as_uint(-INFINITY);
             }
             // row max: eight independent chains of 3-input max, then a short tree
             float mm[8];
