@@ -48,7 +48,7 @@ constexpr uint32_t TMEM_COLS = 512;
 // in the issue loop starves the tensor pipe (its queue holds only a few instructions); below
 // about 88 registers that happened.  128*104 + 256*200 = 384*168, the registers the CTA is
 // launched with (168 per thread).
-constexpr int kCtrlRegs = 104, kSoftmaxRegs = 200;
+constexpr int kCtrlRegs = 88, kSoftmaxRegs = 208;
 constexpr float kRescaleThreshold = 8.0f;   // base-2 units
 
 constexpr uint32_t kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KiB)
@@ -71,9 +71,9 @@ struct TcCfg {
 };
 
 struct Barriers {
-    uint64_t q;
+    uint64_t q_full, q_empty;
     uint64_t full[kMaxStages], empty[kMaxStages];
-    uint64_t s_full[2], p_full[2], o_final[2];
+    uint64_t s_full[2], p_full[2], o_final[2], o_empty[2];
     uint64_t drain;
 };
 
@@ -90,10 +90,49 @@ __device__ __forceinline__ void settle_copies() {
     }
 }
 
+// One work item: 2 x 128 query rows of one (b, q-head), over the key tiles of this CTA's split.
+struct Item {
+    int q0, bh, kvbh, ntiles, n0, n1, n_kv, kt_begin;
+};
+
+// Item of round r for this CTA: rounds walk the item list in snake order (forward on even
+// rounds, backward on odd ones), which pairs heavy causal blocks with light ones.
+__device__ __forceinline__ bool item_at(const AttnProblem &p, int n_qb, int n_items, int r, Item &w) {
+    const int g = (int)gridDim.x;
+    const int c = (r & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const long long it = (long long)r * g + c;
+    if (it >= n_items) return false;
+    const int units = p.B * p.Hq;
+    const int qb_rank = (int)(it / units);
+    w.bh = (int)(it % units);
+    const int qb = p.causal ? (n_qb - 1 - qb_rank) : qb_rank;   // heaviest blocks first
+    w.q0 = qb * 2 * BM;
+    const int grp = p.Hq / p.Hkv;
+    w.kvbh = (w.bh / p.Hq) * p.Hkv + (w.bh % p.Hq) / grp;
+    w.ntiles = (w.q0 + BM < p.Sq) ? 2 : 1;
+    const int n_kt_all = (p.Sk + BN - 1) / BN;
+    const int tps = (n_kt_all + p.splits - 1) / p.splits;
+    w.kt_begin = blockIdx.y * tps;
+    const int kt_end = min(n_kt_all, w.kt_begin + tps);
+    // key tiles each Q tile visits (causal: up to the tile's last row)
+    int e0 = kt_end, e1 = kt_end;
+    if (p.causal) {
+        e0 = min(e0, min(w.q0 + BM - 1, p.Sq - 1) / BN + 1);
+        e1 = min(e1, min(w.q0 + 2 * BM - 1, p.Sq - 1) / BN + 1);
+    }
+    w.n0 = max(0, e0 - w.kt_begin);
+    w.n1 = w.ntiles == 2 ? max(0, e1 - w.kt_begin) : 0;
+    w.n_kv = max(w.n0, w.n1);
+    return true;
+}
+
+// Persistent: each CTA walks its work items (item_at) with one pipeline whose state -- ring
+// position, barrier phases -- carries from item to item, so an item's Q tiles and first K/V
+// tiles load while the previous item finishes.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mv, const AttnProblem p, int n_qb) {
+               const __grid_constant__ CUtensorMap mv, const AttnProblem p, int n_qb, int n_items) {
     using C = TcCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
@@ -104,47 +143,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + C::Q_OFF, sRing = sbase + C::RING_OFF;
-    // ring position of the n-th tile of the stream K0 V0 K1 V1 ...: stage and phase parity
+    // ring position of the n-th tile of the stream K V K V ...: stage and phase parity
     auto stage_of = [](int n) { return n % C::STAGES; };
     auto parity_of = [](int n) { return (n / C::STAGES) & 1; };
-
-    // ------------------------------------------------------------------ work item
-    // (b * Hq + hq, block of 256 query rows); causal blocks are taken heaviest first.
-    const int units = p.B * p.Hq;
-    const int qb_rank = blockIdx.x / units;
-    const int bh = blockIdx.x % units;
-    const int qb = p.causal ? (n_qb - 1 - qb_rank) : qb_rank;
-    const int q0 = qb * 2 * BM;
-    const int G = p.Hq / p.Hkv;
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    const int kvbh = b * p.Hkv + hq / G;
-    const int ntiles = (q0 + BM < p.Sq) ? 2 : 1;
-    const int n_kt_all = (p.Sk + BN - 1) / BN;
-    const int tps = (n_kt_all + p.splits - 1) / p.splits;
-    const int kt_begin = blockIdx.y * tps;
-    const int kt_end = min(n_kt_all, kt_begin + tps);
-    // key tiles each Q tile visits (causal: up to the tile's last row)
-    int e0 = kt_end, e1 = kt_end;
-    if (p.causal) {
-        e0 = min(e0, min(q0 + BM - 1, p.Sq - 1) / BN + 1);
-        e1 = min(e1, min(q0 + 2 * BM - 1, p.Sq - 1) / BN + 1);
-    }
-    const int n0 = max(0, e0 - kt_begin);
-    const int n1 = ntiles == 2 ? max(0, e1 - kt_begin) : 0;
-    const int n_kv = max(n0, n1);
 
     // ------------------------------------------------------------------ set-up
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
     if (tid == 32) {
-        mbar_init(smem_u32(&bars.q), 1);
+        mbar_init(smem_u32(&bars.q_full), 1);
+        mbar_init(smem_u32(&bars.q_empty), 1);
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&bars.full[s]), 1);
             mbar_init(smem_u32(&bars.empty[s]), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&bars.s_full[t]), 1);
-            mbar_init(smem_u32(&bars.p_full[t]), 1);
+            mbar_init(smem_u32(&bars.p_full[t]), 4);     // one arrival per softmax warp
             mbar_init(smem_u32(&bars.o_final[t]), 1);
+            mbar_init(smem_u32(&bars.o_empty[t]), 4);
         }
         mbar_init(smem_u32(&bars.drain), 1);
         abort_flag = 0;
@@ -157,39 +173,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (warp < 4) {
       setmaxnreg_dec<kCtrlRegs>();
-      if ((warp == 0 || warp == 2) && lane == 0 && n_kv > 0) {
+      if ((warp == 0 || warp == 2) && lane == 0) {
         // ============================================================== TMA producers
-        // The ring receives K0 V0 K1 V1 ...; warp 0 issues the Q tiles and the K tiles (even
-        // stream positions), warp 2 the V tiles (odd positions), one TMA instruction per tile,
-        // so neither stream waits behind the other's instruction issue.
+        // The ring receives K V K V ... in consumption order; warp 0 issues the Q tiles and the
+        // K tiles (even stream positions), warp 2 the V tiles (odd positions), one TMA
+        // instruction per tile, so neither stream waits behind the other's instruction issue.
+        // An item's Q tiles load once the previous item's last Q K^T products have completed.
         const int odd = warp == 2;
         const CUtensorMap *map = odd ? &mv : &mk;
         tma_prefetch_desc(map);
-        if (!odd) {
-            tma_prefetch_desc(&mq);
-            mbar_expect_tx(smem_u32(&bars.q), ntiles * C::TILE);
-            for (int t = 0; t < ntiles; ++t)
-                tma_load_4d<false>(sQ + t * C::TILE, &mq, smem_u32(&bars.q), 0, q0 + t * BM, 0, bh);
-        }
+        if (!odd) tma_prefetch_desc(&mq);
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int n = 2 * j + odd;
-            const int st = stage_of(n);
-            ok = mbar_wait(smem_u32(&bars.empty[st]), parity_of(n) ^ 1, &abort_flag);
-            if (!ok) break;
-            mbar_expect_tx(smem_u32(&bars.full[st]), C::TILE);
-            tma_load_4d<false>(sRing + st * C::TILE, map, smem_u32(&bars.full[st]), 0, (kt_begin + j) * BN, 0, kvbh);
+        int gt = 0, qc = 0;   // key tiles streamed so far, Q loads so far
+        Item w;
+        for (int r = 0; ok && item_at(p, n_qb, n_items, r, w); ++r) {
+            if (w.n_kv == 0) continue;
+            if (!odd) {
+                ok = mbar_wait(smem_u32(&bars.q_empty), (qc & 1) ^ 1, &abort_flag);
+                if (!ok) break;
+                ++qc;
+                mbar_expect_tx(smem_u32(&bars.q_full), w.ntiles * C::TILE);
+                for (int t = 0; t < w.ntiles; ++t)
+                    tma_load_4d<false>(sQ + t * C::TILE, &mq, smem_u32(&bars.q_full), 0, w.q0 + t * BM, 0, w.bh);
+            }
+            for (int j = 0; j < w.n_kv; ++j) {
+                const int n = 2 * (gt + j) + odd;
+                const int st = stage_of(n);
+                ok = mbar_wait(smem_u32(&bars.empty[st]), parity_of(n) ^ 1, &abort_flag);
+                if (!ok) break;
+                mbar_expect_tx(smem_u32(&bars.full[st]), C::TILE);
+                tma_load_4d<false>(sRing + st * C::TILE, map, smem_u32(&bars.full[st]), 0, (w.kt_begin + j) * BN, 0,
+                                   w.kvbh);
+            }
+            gt += w.n_kv;
         }
         if (!ok) {
             raise_timeout(&abort_flag, p.status);
             settle_copies();
         }
-      } else if (warp == 1 && lane == 0 && n_kv > 0) {
+      } else if (warp == 1 && lane == 0) {
         // ============================================================== MMA issuer
         // Issue order per key tile i:  O_0 += P_0 V_i;  S_0 = Q_0 K_{i+1}^T;  O_1 += P_1 V_i;
         // S_1 = Q_1 K_{i+1}^T, so one tile's softmax runs while the other tile's products do.
         // Each PV waits for its tile's P; the commit after a tile's S covers the PV before it,
-        // which the softmax relies on when it rescales O.
+        // which the softmax relies on when it rescales O.  An item's first PV of a tile also
+        // waits until the softmax has read that tile's O of the previous item.
         //
         // Descriptors are built once per operand tile; stepping along K adds the byte offset
         // (>> 4) to the start-address field, which cannot carry out of its 14 bits because
@@ -213,57 +241,75 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             for (int k = 0; k < BN / 16; ++k)
                 mma_ts(dst, pa + k * 8, vd + ((k * 2048) >> 4), C::IDESC_PV, acc || k > 0);
         };
-        bool ok = mbar_wait_spin(smem_u32(&bars.q), 0, &abort_flag);
-        if (ok) ok = mbar_wait_spin(smem_u32(&bars.full[0]), 0, &abort_flag);
-        if (ok) {
+        // PV for Q tile t at key tile i of an item; pc[t] counts P handshakes, oe[t] the O
+        // hand-backs owed by earlier items
+        int pc[2] = {0, 0}, oe[2] = {0, 0};
+        auto pv_step = [&](int t, int i, int nt, int sv) -> bool {
+            if (i == 0 && oe[t] > 0 &&
+                !mbar_wait_spin(smem_u32(&bars.o_empty[t]), (oe[t] - 1) & 1, &abort_flag))
+                return false;
+            if (!mbar_wait_spin(smem_u32(&bars.p_full[t]), pc[t] & 1, &abort_flag)) return false;
+            ++pc[t];
+            tc_fence_after();
+            issue_pv(t, sv, i > 0);
+            if (i == nt - 1) mma_commit(smem_u32(&bars.o_final[t]));
+            return true;
+        };
+        bool ok = true;
+        int gt = 0, qc = 0;
+        Item w;
+        for (int r = 0; ok && item_at(p, n_qb, n_items, r, w); ++r) {
+            if (w.n_kv == 0) continue;
+            const int n0 = w.n0, n1 = w.n1, n_kv = w.n_kv;
+            ok = mbar_wait_spin(smem_u32(&bars.q_full), qc & 1, &abort_flag);
+            ++qc;
+            const int sk0 = stage_of(2 * gt);
+            if (ok) ok = mbar_wait_spin(smem_u32(&bars.full[sk0]), parity_of(2 * gt), &abort_flag);
+            if (!ok) break;
             tc_fence_after();
             if (n0 > 0) {
-                issue_s(0, 0);
+                issue_s(0, sk0);
                 mma_commit(smem_u32(&bars.s_full[0]));
             }
             if (n1 > 0) {
-                issue_s(1, 0);
+                issue_s(1, sk0);
                 mma_commit(smem_u32(&bars.s_full[1]));
             }
-            mma_commit(smem_u32(&bars.empty[0]));
-        }
-        for (int i = 0; i < n_kv && ok; ++i) {
-            const int nv = 2 * i + 1, nk = 2 * i + 2;   // stream positions of V_i and K_{i+1}
-            const int sv = stage_of(nv), sk = stage_of(nk);
-            const bool more = i + 1 < n_kv;
-            ok = mbar_wait_spin(smem_u32(&bars.full[sv]), parity_of(nv), &abort_flag);
+            mma_commit(smem_u32(&bars.empty[sk0]));
+            // Q is free once the item's last Q K^T products complete: the next item's Q tiles
+            // then load while this item's last softmax and PV products run.
+            if (n_kv == 1) mma_commit(smem_u32(&bars.q_empty));
+            for (int i = 0; i < n_kv; ++i) {
+                const int nv = 2 * (gt + i) + 1, nk = 2 * (gt + i + 1);   // V_i and K_{i+1}
+                const int sv = stage_of(nv), sk = stage_of(nk);
+                const bool more = i + 1 < n_kv;
+                ok = mbar_wait_spin(smem_u32(&bars.full[sv]), parity_of(nv), &abort_flag);
+                if (!ok) break;
+                if (i < n0 && !(ok = pv_step(0, i, n0, sv))) break;
+                if (more) {
+                    ok = mbar_wait_spin(smem_u32(&bars.full[sk]), parity_of(nk), &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (i + 1 < n0) {
+                        issue_s(0, sk);
+                        mma_commit(smem_u32(&bars.s_full[0]));
+                    }
+                }
+                if (i < n1 && !(ok = pv_step(1, i, n1, sv))) break;
+                mma_commit(smem_u32(&bars.empty[sv]));
+                if (more) {
+                    if (i + 1 < n1) {
+                        issue_s(1, sk);
+                        mma_commit(smem_u32(&bars.s_full[1]));
+                    }
+                    mma_commit(smem_u32(&bars.empty[sk]));
+                    if (i + 2 == n_kv) mma_commit(smem_u32(&bars.q_empty));   // last Q K^T issued
+                }
+            }
             if (!ok) break;
-            if (i < n0) {
-                ok = mbar_wait_spin(smem_u32(&bars.p_full[0]), i & 1, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, sv, i > 0);
-                if (i == n0 - 1) mma_commit(smem_u32(&bars.o_final[0]));
-            }
-            if (more) {
-                ok = mbar_wait_spin(smem_u32(&bars.full[sk]), parity_of(nk), &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                if (i + 1 < n0) {
-                    issue_s(0, sk);
-                    mma_commit(smem_u32(&bars.s_full[0]));
-                }
-            }
-            if (i < n1) {
-                ok = mbar_wait_spin(smem_u32(&bars.p_full[1]), i & 1, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(1, sv, i > 0);
-                if (i == n1 - 1) mma_commit(smem_u32(&bars.o_final[1]));
-            }
-            mma_commit(smem_u32(&bars.empty[sv]));
-            if (more) {
-                if (i + 1 < n1) {
-                    issue_s(1, sk);
-                    mma_commit(smem_u32(&bars.s_full[1]));
-                }
-                mma_commit(smem_u32(&bars.empty[sk]));
-            }
+            oe[0] += n0 > 0;
+            oe[1] += n1 > 0;
+            gt += n_kv;
         }
         if (!ok) raise_timeout(&abort_flag, p.status);
         // every MMA issued above completes before TMEM is released
@@ -275,173 +321,194 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         // ============================================================== softmax
         const int t = (warp - 4) >> 2;           // Q tile
         const int r = tid - 128 * (t + 1);       // row within the tile == TMEM lane
-        const int row = q0 + t * BM + r;
-        const int row_first = q0 + t * BM;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t s_addr = lane_base + (t ? C::S_COL1 : C::S_COL0);
         const uint32_t o_addr = lane_base + (t ? C::O_COL1 : C::O_COL0);
-        const int nt = t ? n1 : n0;
         const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY, l = 0.f;
+        const long long rows_total = (long long)p.B * p.Hq * p.Sq;
         bool ok = true;
-        for (int i = 0; i < nt; ++i) {
-            ok = mbar_wait(smem_u32(&bars.s_full[t]), i & 1, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[4][32];
+        int sc = 0, oc = 0;   // S handshakes and finished O tiles so far
+        Item w;
+        for (int rr = 0; ok && item_at(p, n_qb, n_items, rr, w); ++rr) {
+            const int nt = t ? w.n1 : w.n0;
+            const int row_first = w.q0 + t * BM;   // first row of this tile
+            const int row = row_first + r;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int i = 0; i < nt; ++i) {
+                ok = mbar_wait(smem_u32(&bars.s_full[t]), sc & 1, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++sc;
+                tc_fence_after();
+                uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-            tmem_ld_wait();
-            const int key0 = (kt_begin + i) * BN;
-            const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > row_first);
-            if (need_mask) {
-                // column j of the tile (key key0 + j) is kept iff j < lim: inside the sequence
-                // and, when causal, not after this row
-                int lim = p.Sk - key0;
-                if (p.causal) lim = min(lim, row - key0 + 1);
+                for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+                tmem_ld_wait();
+                const int key0 = (w.kt_begin + i) * BN;
+                const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > row_first);
+                if (need_mask) {
+                    // column j of the tile (key key0 + j) is kept iff j < lim: inside the sequence
+                    // and, when causal, not after this row
+                    int lim = p.Sk - key0;
+                    if (p.causal) lim = min(lim, row - key0 + 1);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        if (c * 32 + k >= lim) sr[c][k] = __float_as_uint(-INFINITY);
-            }
-            // row max: eight independent chains of 3-input max, then a short tree
-            float mm[8];
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const int c = g >> 1, k0 = (g & 1) * 16;
-                mm[g] = fmaxf(__uint_as_float(sr[c][k0]), __uint_as_float(sr[c][k0 + 1]));
-#pragma unroll
-                for (int v = 1; v < 8; ++v)
-                    mm[g] = fmax3(mm[g], __uint_as_float(sr[c][k0 + 2 * v]), __uint_as_float(sr[c][k0 + 2 * v + 1]));
-            }
-            const float mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[7]));
-            const float m_tile = mx * sl2;   // -inf stays -inf (sl2 > 0)
-            const float m_new = fmaxf(m_ref, m_tile);
-            const bool rescale = __any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold);
-            float alpha = 1.f;
-            if (rescale) {
-                alpha = ex2_approx(m_ref - m_new);   // m_ref == -inf -> 0
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-            const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mr, -mr);
-            uint64_t acc[4];
-            // p = 2^(s * scale * log2e - m): pairs through one f32x2 FMA, sums in four
-            // independent f32x2 accumulators; P packed to bf16 over the first half of S.
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                acc[c] = f2_pack(0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float p0, p1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * k]), __uint_as_float(sr[c][2 * k + 1])), sc2, nm2),
-                              p0, p1);
-                    p0 = ex2_approx(p0);
-                    p1 = ex2_approx(p1);
-                    acc[c] = f2_add(acc[c], f2_pack(p0, p1));
-                    sr[c][k] = pack_bf16x2(p0, p1);
+                        for (int k = 0; k < 32; ++k)
+                            if (c * 32 + k >= lim) sr[c][k] = __float_as_uint(-INFINITY);
                 }
-                tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
-                          sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
-                          sr[c][15]);
-            }
-            float rs;
-            {
-                const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-                float lo, hi;
-                f2_unpack(a2, lo, hi);
-                rs = lo + hi;
-            }
-            if (rescale && i > 0) {
-                // O_t += P V of earlier tiles has completed: the commit that signalled s_full
-                // for this tile covers every MMA issued before it.  The PV MMA of this tile
-                // waits for p_full, signalled below, after the rescaled O is stored.
-                const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(o_addr + c * 32, o);
-                    tmem_ld_wait();
+                // row max: eight independent chains of 3-input max, then a short tree
+                float mm[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int c = g >> 1, k0 = (g & 1) * 16;
+                    mm[g] = fmaxf(__uint_as_float(sr[c][k0]), __uint_as_float(sr[c][k0 + 1]));
+#pragma unroll
+                    for (int v = 1; v < 8; ++v)
+                        mm[g] = fmax3(mm[g], __uint_as_float(sr[c][k0 + 2 * v]), __uint_as_float(sr[c][k0 + 2 * v + 1]));
+                }
+                const float mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[7]));
+                const float m_tile = mx * sl2;   // -inf stays -inf (sl2 > 0)
+                const float m_new = fmaxf(m_ref, m_tile);
+                const bool rescale = __any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold);
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = ex2_approx(m_ref - m_new);   // m_ref == -inf -> 0
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+                const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mr, -mr);
+                uint64_t acc[4];
+                // p = 2^(s * scale * log2e - m): pairs through one f32x2 FMA, sums in four
+                // independent f32x2 accumulators; P packed to bf16 over the first half of S.
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    acc[c] = f2_pack(0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        float a, bb;
-                        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2), a, bb);
-                        o[2 * k] = __float_as_uint(a);
-                        o[2 * k + 1] = __float_as_uint(bb);
+                        float p0, p1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * k]), __uint_as_float(sr[c][2 * k + 1])), sc2, nm2),
+                                  p0, p1);
+                        p0 = ex2_approx(p0);
+                        p1 = ex2_approx(p1);
+                        acc[c] = f2_add(acc[c], f2_pack(p0, p1));
+                        sr[c][k] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st32(o_addr + c * 32, o);
+                    tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
+                              sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
+                              sr[c][15]);
+                }
+                float rs;
+                {
+                    const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+                    float lo, hi;
+                    f2_unpack(a2, lo, hi);
+                    rs = lo + hi;
+                }
+                if (rescale && i > 0) {
+                    // O_t += P V of earlier tiles has completed: the commit that signalled s_full
+                    // for this tile covers every MMA issued before it.  The PV MMA of this tile
+                    // waits for p_full, signalled below, after the rescaled O is stored.
+                    const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            float a, bb;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2), a, bb);
+                            o[2 * k] = __float_as_uint(a);
+                            o[2 * k + 1] = __float_as_uint(bb);
+                        }
+                        tmem_st32(o_addr + c * 32, o);
+                    }
+                }
+                l += rs;
+                // this warp's 32 rows of P (and any rescaled O) are in TMEM
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[t]));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            if (t < w.ntiles) {
+                const bool have_o = nt > 0;
+                if (have_o) {
+                    ok = mbar_wait(smem_u32(&bars.o_final[t]), oc & 1, &abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ++oc;
+                    tc_fence_after();
+                }
+                const long long grow = (long long)w.bh * p.Sq + row;
+                const bool row_ok = row < p.Sq;
+                if (p.splits == 1) {
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + grow * D;
+                    // rows are D * 2 bytes apart, so a 32-byte aligned O gives 32-byte aligned chunks
+                    const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        if (have_o) {
+                            tmem_ld32(o_addr + c * 32, o);
+                            tmem_ld_wait();
+                        }
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            pk[k] = have_o ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv)
+                                           : 0u;
+                        if (row_ok) {
+                            if (o32) {
+                                st_global_v8(Og + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+                                st_global_v8(Og + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+                            } else {
+                                uint4 *dst = reinterpret_cast<uint4 *>(Og + c * 32);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                            }
+                        }
+                    }
+                    if (p.lse && row_ok) p.lse[grow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                } else {
+                    float *A = p.part_acc + ((size_t)blockIdx.y * rows_total + grow) * D;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        if (have_o) {
+                            tmem_ld32(o_addr + c * 32, o);
+                            tmem_ld_wait();
+                        }
+                        if (row_ok) {
+                            float4 *dst = reinterpret_cast<float4 *>(A + c * 32);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                dst[k] = have_o ? make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                              __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    if (row_ok) {
+                        p.part_m[(size_t)blockIdx.y * rows_total + grow] = have_o ? m_ref : -INFINITY;
+                        p.part_l[(size_t)blockIdx.y * rows_total + grow] = have_o ? l : 0.f;
+                    }
+                }
+                if (have_o) {
+                    // this warp's rows of O_t are in registers: the next item's first PV may
+                    // overwrite them
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars.o_empty[t]));
                 }
             }
-            l += rs;
-            // P (and any rescaled O) of all 128 rows are in TMEM: one arrival for the tile.
-            tmem_st_wait();
-            tc_fence_before();
-            named_barrier(1 + t, 128);
-            if (r == 0) mbar_arrive(smem_u32(&bars.p_full[t]));
         }
         if (!ok) raise_timeout(&abort_flag, p.status);
-        // ---------------------------------------------------------- epilogue
-        if (t < ntiles) {
-            bool have_o = false;
-            if (ok && nt > 0) {
-                ok = mbar_wait(smem_u32(&bars.o_final[t]), 0, &abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) raise_timeout(&abort_flag, p.status);
-                have_o = ok;
-                tc_fence_after();
-            }
-            const long long rows_total = (long long)p.B * p.Hq * p.Sq;
-            const long long grow = (long long)bh * p.Sq + row;
-            const bool row_ok = row < p.Sq;
-            if (p.splits == 1) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + grow * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    if (have_o) {
-                        tmem_ld32(o_addr + c * 32, o);
-                        tmem_ld_wait();
-                    }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        pk[k] = have_o ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv)
-                                       : 0u;
-                    if (row_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(Og + c * 32);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                    }
-                }
-                if (p.lse && row_ok) p.lse[grow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-            } else {
-                float *A = p.part_acc + ((size_t)blockIdx.y * rows_total + grow) * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    if (have_o) {
-                        tmem_ld32(o_addr + c * 32, o);
-                        tmem_ld_wait();
-                    }
-                    if (row_ok) {
-                        float4 *dst = reinterpret_cast<float4 *>(A + c * 32);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            dst[k] = have_o ? make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                                          __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-                if (row_ok) {
-                    p.part_m[(size_t)blockIdx.y * rows_total + grow] = have_o ? m_ref : -INFINITY;
-                    p.part_l[(size_t)blockIdx.y * rows_total + grow] = have_o ? l : 0.f;
-                }
-            }
-        }
     }
 
     tc_fence_before();
@@ -455,7 +522,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
 // ------------------------------------------------------------------------- host side
 template <int D>
-cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
+cudaError_t launch_t(const AttnProblem &p, int sm_count, cudaStream_t s) {
     using C = TcCfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -470,9 +537,12 @@ cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
         !make_bf16_tile_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, BN))
         return cudaErrorInvalidValue;
     const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
-    const long long ctas = (long long)n_qb * p.B * p.Hq;
-    if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;
-    attn_tc_kernel<D><<<dim3((unsigned)ctas, (unsigned)p.splits), NTHREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p, n_qb);
+    const long long items = (long long)n_qb * p.B * p.Hq;
+    if (items >= (1LL << 31)) return cudaErrorInvalidValue;
+    // one resident CTA per SM walks the items; fewer items than SMs: one CTA per item
+    const int grid = (int)(items < sm_count ? items : (sm_count > 0 ? sm_count : 1));
+    attn_tc_kernel<D><<<dim3((unsigned)grid, (unsigned)p.splits), NTHREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p, n_qb,
+                                                                                                 (int)items);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -502,8 +572,7 @@ int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {
 }
 
 cudaError_t launch_attn_tc(const AttnProblem &p, int sm_count, cudaStream_t s) {
-    (void)sm_count;
-    cudaError_t e = p.D == 64 ? launch_t<64>(p, s) : launch_t<128>(p, s);
+    cudaError_t e = p.D == 64 ? launch_t<64>(p, sm_count, s) : launch_t<128>(p, sm_count, s);
     if (e == cudaSuccess && p.splits > 1) e = launch_attn_combine(p, s);
     return e;
 }

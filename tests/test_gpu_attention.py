@@ -119,6 +119,31 @@ def test_gqa_causal_prefill_full_size_sampled(osf):
     assert torch.isfinite(o.float()).all()
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_gqa_more_items_than_sms(osf, causal):
+    """More (b, head, 256-row block) work items than SMs, with a ragged last block: each CTA
+    of the tensor-core prefill walks several items and carries its pipeline across them."""
+    B, Hq, Hkv, S, D = 2, 40, 8, 1000, 128
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=21 + causal, dtype="bf16")
+    lse = torch.empty(B, Hq, S, device="cuda")
+    o = osf.osf_attn_fwd_gqa(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), causal=causal, lse=lse)
+    ref, ref_lse = oracle.attention_gqa(*(si.bf16_bits_to_f32(a) for a in (q, k, v)), causal=causal)
+    check(o, ref, "bf16", f"gqa many items causal={causal}")
+    assert_f32_close(lse.cpu().numpy(), ref_lse, atol=1e-3, what="lse")
+
+
+def test_output_16_byte_aligned_only(osf):
+    """An output that starts 16 bytes past a 32-byte boundary takes the 16-byte store path."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 300, 128
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=23, dtype="bf16")
+    n = B * Hq * S * D
+    out = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")[8:].view(B, Hq, S, D)
+    assert out.data_ptr() % 32 == 16
+    osf.osf_attn_fwd_gqa(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), out=out, causal=True)
+    ref, _ = oracle.attention_gqa(*(si.bf16_bits_to_f32(a) for a in (q, k, v)), causal=True)
+    check(out, ref, "bf16", "16-byte aligned output")
+
+
 # ----------------------------------------------------------------------------- decode
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("splits", [1, 2, 7, 0])
