@@ -398,6 +398,24 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(vals, world, device):
+    """Element-wise maximum of per-rank values over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return [float(v) for v in vals]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(world, amount_per_rank, total_ms, steps):
+    """Whole-job throughput: every rank processes `amount_per_rank` units per step (weak
+    scaling), and a step lasts as long as the slowest rank's (already reduced) time."""
+    mean_ms = total_ms / steps
+    return world * amount_per_rank / (mean_ms / 1e3), mean_ms
+
+
 def reference_arm(args, world, rank):
     w = WORKLOADS[args.workload]
     if rank != 0:
@@ -463,16 +481,8 @@ def main():
     sampler.start()
     res = measure(args.workload, w, osf, dev, args.steps, args.warmup, flush, barrier, sampler)
     sampler.stop()
-    mean_ms = statistics.mean(res["ms"])
-    total_ms = sum(res["ms"])
-    e2e_ms = statistics.mean(res["e2e_ms"])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-        mean_ms = total_ms / args.steps
-    value = world * res["amount"] / (mean_ms / 1e3)
+    total_ms, e2e_ms = max_over_ranks([sum(res["ms"]), statistics.mean(res["e2e_ms"])], world, dev)
+    value, mean_ms = job_rate(world, res["amount"], total_ms, args.steps)
     rl = roofline(res, pk, w)
     rl["peak_source"] = pk_src + (" burst" if rl["bound"] == "tensor" else "")
 
@@ -503,7 +513,7 @@ def main():
                        "inputs": "seeded i.i.d. N(0,1) (SplitMix64 + Box-Muller), resident in HBM",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": rl, "cpu_baseline": cpu,
-            "e2e": {"value": round(world * res["amount"] / (e2e_ms / 1e3), 3), "unit": res["unit"],
+            "e2e": {"value": round(job_rate(world, res["amount"], e2e_ms, 1)[0], 3), "unit": res["unit"],
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                     "ms_per_step": round(e2e_ms, 5)},
             "gpu_launches": res["launches"], "launches_per_step": res["launches_per_call"],
