@@ -66,8 +66,8 @@ SM_COUNT_GB300 = 152
 # each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
 # source that changed since the capture reports null.
 TRAFFIC = {
-    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "63748d2e3eb2c825",
-                           "bytes": 134.56e6, "scope": "attn_tc_kernel<128>, one launch"},
+    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "aa1f901aa51729d2",
+                           "bytes": 136.80e6, "scope": "attn_tc_kernel<128>, one launch"},
     "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "f0dd5302023a97d4",
                    "bytes": 1079.81e6, "scope": "decode_kernel<128>, one launch"},
     "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "1369193089605318",
