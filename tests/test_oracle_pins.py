@@ -359,3 +359,66 @@ def test_lse_matches_scipy_logsumexp():
     S = Q @ K.T * 0.25
     for i in range(9):
         assert abs(lse[i] - sp.logsumexp(S[i, :i + 1])) < 1e-13
+
+
+# ------------------------------------------------------------- mask alignment when Sq != Sk
+@pytest.mark.parametrize("Sq,Sk", [(5, 5), (3, 11), (7, 4), (1, 9)])
+def test_masked_rows_equal_unmasked_attention_on_the_key_prefix(Sq, Sk):
+    """Each masked row is plain (unmasked) attention over the keys it may see: keys 0..i for
+    top-left ([Q3] "自注意力原理", tril(ones(Sq, Sk))), 0..i + Sk - Sq for bottom-right."""
+    rng = np.random.default_rng(Sq * 31 + Sk)
+    B, Hq, Hkv, D = 1, 4, 2, 8
+    Q = rng.standard_normal((B, Hq, Sq, D))
+    K = rng.standard_normal((B, Hkv, Sk, D))
+    V = rng.standard_normal((B, Hkv, Sk, D))
+    for mask, off in (("top_left", 0), ("bottom_right", Sk - Sq)):
+        O, lse = oracle.attention_gqa(Q, K, V, mask=mask)
+        for hq in range(Hq):
+            kvh = hq // (Hq // Hkv)
+            for i in range(Sq):
+                last = Sk - 1 if (mask == "top_left" and Sq == 1) else min(i + off, Sk - 1)
+                if last < 0:
+                    assert np.all(O[0, hq, i] == 0) and lse[0, hq, i] == -np.inf
+                    continue
+                o, l = oracle.attention(Q[0, hq, i:i + 1], K[0, kvh, :last + 1], V[0, kvh, :last + 1])
+                np.testing.assert_allclose(O[0, hq, i], o[0], rtol=1e-13, atol=1e-13)
+                assert abs(lse[0, hq, i] - l[0]) < 1e-12
+
+
+def test_bottom_right_equals_top_left_when_square_and_no_mask_for_one_row():
+    rng = np.random.default_rng(5)
+    Q = rng.standard_normal((2, 2, 6, 4)); K = rng.standard_normal((2, 1, 6, 4)); V = rng.standard_normal((2, 1, 6, 4))
+    a = oracle.attention_gqa(Q, K, V, mask="bottom_right")
+    b = oracle.attention_gqa(Q, K, V, causal=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    q1 = Q[:, :, :1]
+    c = oracle.attention_gqa(q1, K, V, mask="bottom_right")
+    d = oracle.attention_gqa(q1, K, V, mask="none")
+    assert np.array_equal(c[0], d[0])
+
+
+def test_bottom_right_brute_force_loops():
+    """Bottom-right alignment by explicit loops (exp of each kept score over their sum)."""
+    rng = np.random.default_rng(8)
+    Sq, Sk, D = 3, 5, 2
+    Q = rng.standard_normal((1, 1, Sq, D)); K = rng.standard_normal((1, 1, Sk, D)); V = rng.standard_normal((1, 1, Sk, D))
+    O, lse = oracle.attention_gqa(Q, K, V, mask="bottom_right")
+    for i in range(Sq):
+        keep = [j for j in range(Sk) if j <= i + Sk - Sq]
+        sc = [sum(Q[0, 0, i, t] * K[0, 0, j, t] for t in range(D)) / math.sqrt(D) for j in keep]
+        mx = max(sc)
+        w = [math.exp(x - mx) for x in sc]
+        for c in range(D):
+            ref = sum(wj * V[0, 0, j, c] for wj, j in zip(w, keep)) / sum(w)
+            assert abs(O[0, 0, i, c] - ref) < 1e-13
+        assert abs(lse[0, 0, i] - (mx + math.log(sum(w)))) < 1e-13
+
+
+def test_attention_rows_follows_the_mask():
+    rng = np.random.default_rng(9)
+    Q = rng.standard_normal((1, 2, 4, 8)); K = rng.standard_normal((1, 1, 9, 8)); V = rng.standard_normal((1, 1, 9, 8))
+    full, full_lse = oracle.attention_gqa(Q, K, V, mask="bottom_right")
+    rows = [(0, h, i) for h in range(2) for i in range(4)]
+    o, l = oracle.attention_rows(Q, K, V, rows, mask="bottom_right")
+    np.testing.assert_allclose(o, np.stack([full[0, h, i] for _, h, i in rows]), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(l, np.array([full_lse[0, h, i] for _, h, i in rows]), rtol=1e-13)
