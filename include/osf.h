@@ -97,6 +97,40 @@ int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int d
                      int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                      float *lse, void *workspace, size_t workspace_bytes, osf_stream stream);
 
+/* Mask modes of osf_attn_fwd_gqa_ex. */
+typedef enum {
+    OSF_MASK_NONE = 0,          /* every key */
+    OSF_MASK_TOP_LEFT = 1,      /* Sq > 1: row i sees keys 0..i (tril(ones(Sq, Sk)), [Q3] "自注意力原理");
+                                   Sq == 1: every key, as on the page */
+    OSF_MASK_BOTTOM_RIGHT = 2   /* row i sees keys 0..i + Sk - Sq: the Sq new rows follow a cache of
+                                   Sk - Sq keys (not on the pages; equals TOP_LEFT when Sq == Sk) */
+} osf_mask;
+
+/*
+ * osf_attn_fwd_gqa_ex -- osf_attn_fwd_gqa on strided tensors, with a mask mode.
+ * The operation is the one of osf_attn_fwd_gqa, [Q3] "自注意力原理" + "GQA".  [Q3] "stride的作用":
+ * a head split or a transpose of any but the last dimension only changes strides, and an
+ * expanded (broadcast) dimension has stride 0; so every tensor is addressed through its own
+ * element strides instead of being copied to [B, H, S, D] first.
+ *
+ * strides: NULL (all four tensors contiguous [B, H, S, D]) or 12 element strides, in order
+ *     Q: b, h, s   K: b, h, s   V: b, h, s   O: b, h, s.
+ *     The d stride is 1.  E.g. a [B, S, H, D] tensor has b = S*H*D, h = D, s = H*D.
+ *     Strides must be >= 0 (0 broadcasts an input); O's rows must not overlap one another,
+ *     and O must not overlap Q, K, V or lse (checked on address ranges) -> else OSF_ERR_INVALID.
+ * mask: an osf_mask; any Sq, Sk.  A row that sees no key (BOTTOM_RIGHT with i < Sq - Sk)
+ *     gets O = 0 and lse = -inf.
+ * lse: optional contiguous float32 [B, Hq, Sq], natural-log log-sum-exp of each row.
+ * Workspace: osf_attn_workspace_bytes with the same dtype and sizes gives enough.
+ * Kernel choice as in osf_attn_fwd_gqa.  The TMA kernels need 16-byte aligned bases and
+ * strides (multiples of 8 bf16 elements); other layouts run on the CUDA-core kernel.
+ * Errors, emptiness and ownership as in osf_attn_fwd_gqa.
+ */
+int osf_attn_fwd_gqa_ex(const void *Q, const void *K, const void *V, void *O, int dtype,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int D, const long long *strides,
+                        int mask, float scale, float *lse, void *workspace, size_t workspace_bytes,
+                        osf_stream stream);
+
 /* Bytes of workspace osf_attn_fwd_gqa needs for these arguments (written to *bytes). */
 int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D,
                              size_t *bytes);

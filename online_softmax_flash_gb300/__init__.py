@@ -17,7 +17,7 @@ __all__ = [
     "osf_status_string", "osf_version", "osf_sm_count", "osf_attn_fwd", "osf_attn_fwd_gqa",
     "osf_attn_workspace_bytes", "osf_attn_decode_gqa", "osf_attn_decode_workspace_bytes",
     "osf_softmax_rows", "osf_softmax_workspace_bytes", "osf_device_status", "osf_launch_count",
-    "solve",
+    "solve", "osf_attn_fwd_gqa_ex", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
 ]
 
 OSF_OK, OSF_ERR_INVALID, OSF_ERR_UNSUPPORTED, OSF_ERR_CUDA, OSF_ERR_TIMEOUT, OSF_ERR_WORKSPACE = range(6)
@@ -35,6 +35,7 @@ _SIGS = {
     "osf_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "osf_attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "osf_attn_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "osf_attn_fwd_gqa_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "osf_attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
     "osf_attn_decode_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "osf_softmax_rows": (_i, [_vp, _vp, _ll, _ll, _vp, _sz, _vp]),
@@ -79,11 +80,11 @@ def _stream(dev) -> int:
     return torch.cuda.current_stream(dev).cuda_stream
 
 
-def _need_cuda(*ts) -> None:
+def _need_cuda(*ts, contiguous: bool = True) -> None:
     for t in ts:
         if t is not None and not t.is_cuda:
             raise ValueError("libosf works on CUDA tensors only (no CPU path)")
-        if t is not None and not t.is_contiguous():
+        if contiguous and t is not None and not t.is_contiguous():
             raise ValueError("libosf expects contiguous row-major tensors")
 
 
@@ -151,6 +152,40 @@ def osf_attn_fwd_gqa(q, k, v, out=None, causal: bool = False, scale: float | Non
                                   int(bool(causal)), 0.0 if scale is None else float(scale),
                                   _ptr(lse), _ptr(ws), ws_bytes, _stream(q.device)),
            "osf_attn_fwd_gqa")
+    return out
+
+
+OSF_MASK_NONE, OSF_MASK_TOP_LEFT, OSF_MASK_BOTTOM_RIGHT = 0, 1, 2
+_MASKS = {"none": OSF_MASK_NONE, "top_left": OSF_MASK_TOP_LEFT, "bottom_right": OSF_MASK_BOTTOM_RIGHT}
+
+
+def osf_attn_fwd_gqa_ex(q, k, v, out=None, mask="none", scale: float | None = None, lse=None,
+                        workspace=None):
+    """Grouped-query attention on logical [B, H, S, D] views with any strides (the last
+    dimension contiguous), e.g. ``x.transpose(1, 2)`` of a [B, S, H, D] tensor; ``mask`` is
+    "none", "top_left", "bottom_right" (or an OSF_MASK_* code).  ``out`` defaults to a
+    contiguous [B, Hq, Sq, D] tensor; ``lse`` must be a contiguous float32 [B, Hq, Sq]."""
+    _need_cuda(q, k, v, out, lse, contiguous=False)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=q.dtype, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dim() != 4 or (t.shape[3] > 1 and t.stride(3) != 1):
+            raise ValueError(f"{name} must be a 4-D [B, H, S, D] view with a contiguous last dimension")
+    if lse is not None and not lse.is_contiguous():
+        raise ValueError("lse must be contiguous")
+    st = (ctypes.c_longlong * 12)(*(int(t.stride(i)) for t in (q, k, v, out) for i in range(3)))
+    m = _MASKS[mask] if isinstance(mask, str) else int(mask)
+    ws_n = osf_attn_workspace_bytes(dt, B, Hq, Hkv, Sq, Sk, D)
+    ws = _workspace(ws_n, q.device, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().osf_attn_fwd_gqa_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), dt, B, Hq, Hkv, Sq, Sk, D,
+                                     ctypes.cast(st, ctypes.c_void_p), m,
+                                     0.0 if scale is None else float(scale), _ptr(lse), _ptr(ws), ws_bytes,
+                                     _stream(q.device)),
+           "osf_attn_fwd_gqa_ex")
     return out
 
 

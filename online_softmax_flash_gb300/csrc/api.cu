@@ -65,42 +65,110 @@ size_t elem_size(int dtype) { return dtype == OSF_F32 ? 4 : 2; }
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? OSF_OK : OSF_ERR_CUDA; }
 
-// Shared validation of the GQA problem; fills `p` (without workspace pointers).
-int check_gqa(const void *Q, const void *K, const void *V, void *O, int dtype, int B, int Hq,
-              int Hkv, int Sq, int Sk, int D, int causal, float scale, float *lse,
-              AttnProblem &p, bool &empty) {
+// Bytes spanned by a strided [n0, n1, n2, D] tensor (strides s0..s2 in elements, d contiguous).
+size_t span_bytes(long long n0, long long n1, long long n2, long long D, long long s0, long long s1,
+                  long long s2, size_t es) {
+    return (size_t)((n0 - 1) * s0 + (n1 - 1) * s1 + (n2 - 1) * s2 + D) * es;
+}
+
+// True when no two rows of a [n0, n1, n2, D] tensor with these strides share an element: the
+// dimensions, sorted by stride, each step over the whole block of the smaller ones.
+bool rows_disjoint(long long n0, long long n1, long long n2, long long D, long long s0, long long s1,
+                   long long s2) {
+    long long st[3] = {s0, s1, s2}, n[3] = {n0, n1, n2};
+    for (int i = 0; i < 3; ++i)
+        for (int j = i + 1; j < 3; ++j)
+            if (st[j] < st[i]) {
+                long long t = st[i]; st[i] = st[j]; st[j] = t;
+                t = n[i]; n[i] = n[j]; n[j] = t;
+            }
+    long long block = D;
+    for (int i = 0; i < 3; ++i) {
+        if (n[i] <= 1) continue;
+        if (st[i] < block) return false;
+        block = st[i] * (n[i] - 1) + block;
+    }
+    return true;
+}
+
+// Shared validation of the GQA problem; fills `p` (without workspace pointers).  `strides`:
+// NULL (contiguous [B, H, S, D]) or Q, K, V, O x (b, h, s) element strides.  `mask`: an
+// osf_mask; the original entry point passes TOP_LEFT for causal and keeps its Sq == Sk rule.
+int check_gqa_ex(const void *Q, const void *K, const void *V, void *O, int dtype, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int D, const long long *strides, int mask, float scale,
+                 float *lse, AttnProblem &p, bool &empty) {
     empty = false;
     if (dtype != OSF_F32 && dtype != OSF_BF16) return OSF_ERR_INVALID;
     if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Sk < 0 || D <= 0) return OSF_ERR_INVALID;
     if (Hq == 0 || Hkv == 0 || Hq % Hkv != 0) return OSF_ERR_INVALID;
     if (!(scale == scale)) return OSF_ERR_INVALID;  // NaN
-    if (causal && Sq > 1 && Sq != Sk) return OSF_ERR_INVALID;
+    if (mask != OSF_MASK_NONE && mask != OSF_MASK_TOP_LEFT && mask != OSF_MASK_BOTTOM_RIGHT)
+        return OSF_ERR_INVALID;
+    long long st[12];
+    if (strides) {
+        for (int i = 0; i < 12; ++i) {
+            if (strides[i] < 0) return OSF_ERR_INVALID;
+            st[i] = strides[i];
+        }
+    } else {
+        const long long q[3] = {(long long)Hq * Sq * D, (long long)Sq * D, D};
+        const long long kv[3] = {(long long)Hkv * Sk * D, (long long)Sk * D, D};
+        for (int i = 0; i < 3; ++i) {
+            st[i] = q[i];
+            st[3 + i] = kv[i];
+            st[6 + i] = kv[i];
+            st[9 + i] = q[i];
+        }
+    }
     if (D > 256) return OSF_ERR_UNSUPPORTED;
     if (B == 0 || Sq == 0 || Sk == 0) { empty = true; return OSF_OK; }
     // per-head element counts index with 32-bit row numbers inside kernels
     if ((long long)Sq * D >= (1LL << 31) || (long long)Sk * D >= (1LL << 31) ||
         (long long)B * Hq >= (1LL << 31) || (long long)B * Hq * Sq >= (1LL << 40))
         return OSF_ERR_UNSUPPORTED;
+    for (int i = 0; i < 12; ++i)
+        if (st[i] >= (1LL << 40)) return OSF_ERR_UNSUPPORTED;
     if (!Q || !K || !V || !O) return OSF_ERR_INVALID;
     const size_t es = elem_size(dtype);
-    const size_t nq = (size_t)B * Hq * Sq * D * es, nkv = (size_t)B * Hkv * Sk * D * es;
-    if (overlaps(O, nq, Q, nq) || overlaps(O, nq, K, nkv) || overlaps(O, nq, V, nkv))
+    const size_t nq = span_bytes(B, Hq, Sq, D, st[0], st[1], st[2], es);
+    const size_t nk = span_bytes(B, Hkv, Sk, D, st[3], st[4], st[5], es);
+    const size_t nv = span_bytes(B, Hkv, Sk, D, st[6], st[7], st[8], es);
+    const size_t no = span_bytes(B, Hq, Sq, D, st[9], st[10], st[11], es);
+    if (!rows_disjoint(B, Hq, Sq, D, st[9], st[10], st[11])) return OSF_ERR_INVALID;
+    if (overlaps(O, no, Q, nq) || overlaps(O, no, K, nk) || overlaps(O, no, V, nv))
         return OSF_ERR_INVALID;
     if (lse) {
         const size_t nl = (size_t)B * Hq * Sq * sizeof(float);
-        if (overlaps(lse, nl, O, nq) || overlaps(lse, nl, Q, nq) || overlaps(lse, nl, K, nkv) ||
-            overlaps(lse, nl, V, nkv))
+        if (overlaps(lse, nl, O, no) || overlaps(lse, nl, Q, nq) || overlaps(lse, nl, K, nk) ||
+            overlaps(lse, nl, V, nv))
             return OSF_ERR_INVALID;
     }
     p = AttnProblem{};
     p.q = Q; p.k = K; p.v = V; p.o = O; p.lse = lse;
     p.dtype = dtype;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Sk = Sk; p.D = D;
-    p.causal = (causal && Sq > 1) ? 1 : 0;
+    p.q_sb = st[0]; p.q_sh = st[1]; p.q_ss = st[2];
+    p.k_sb = st[3]; p.k_sh = st[4]; p.k_ss = st[5];
+    p.v_sb = st[6]; p.v_sh = st[7]; p.v_ss = st[8];
+    p.o_sb = st[9]; p.o_sh = st[10]; p.o_ss = st[11];
+    // key j is visible to row i iff j <= i + off; a mask that hides nothing is dropped
+    const long long off = mask == OSF_MASK_BOTTOM_RIGHT ? (long long)Sk - Sq : 0;
+    const bool masks = (mask == OSF_MASK_TOP_LEFT && Sq > 1) || mask == OSF_MASK_BOTTOM_RIGHT;
+    p.causal = (masks && off < (long long)Sk - 1) ? 1 : 0;
+    p.causal_off = p.causal ? (int)off : 0;
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = sc * kLog2e;
     p.splits = 1;
     return OSF_OK;
+}
+
+int check_gqa(const void *Q, const void *K, const void *V, void *O, int dtype, int B, int Hq,
+              int Hkv, int Sq, int Sk, int D, int causal, float scale, float *lse,
+              AttnProblem &p, bool &empty) {
+    // the original entry point: contiguous tensors, causal only with Sq == Sk (or Sq == 1)
+    if (causal && Sq > 1 && Sq != Sk) return OSF_ERR_INVALID;
+    return check_gqa_ex(Q, K, V, O, dtype, B, Hq, Hkv, Sq, Sk, D, nullptr,
+                        causal ? OSF_MASK_TOP_LEFT : OSF_MASK_NONE, scale, lse, p, empty);
 }
 
 // Workspace layout for split partial states: acc | m | l (floats), 256-byte aligned pieces.
@@ -243,6 +311,21 @@ int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int d
     AttnProblem p;
     bool empty;
     int st = check_gqa(Q, K, V, O, dtype, B, Hq, Hkv, Sq, Sk, D, causal, scale, lse, p, empty);
+    if (st != OSF_OK || empty) return st;
+    DeviceInfo *dev;
+    if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    const Path path = choose_path(p, Q, K, V, O);
+    const int splits = plan_splits(p, path, dev->sm_count, 0);
+    return run_gqa(p, path, workspace, workspace_bytes, splits, dev, (cudaStream_t)stream);
+}
+
+int osf_attn_fwd_gqa_ex(const void *Q, const void *K, const void *V, void *O, int dtype, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int D, const long long *strides, int mask,
+                        float scale, float *lse, void *workspace, size_t workspace_bytes,
+                        osf_stream stream) {
+    AttnProblem p;
+    bool empty;
+    int st = check_gqa_ex(Q, K, V, O, dtype, B, Hq, Hkv, Sq, Sk, D, strides, mask, scale, lse, p, empty);
     if (st != OSF_OK || empty) return st;
     DeviceInfo *dev;
     if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;

@@ -58,20 +58,20 @@ attn_simt_kernel(const AttnProblem p) {
     const int q0 = qt * BM;
     const int D = p.D;
 
-    const T *Qg = static_cast<const T *>(p.q) + ((size_t)bh * p.Sq + q0) * D;
-    const T *Kg = static_cast<const T *>(p.k) + ((size_t)b * p.Hkv + kvh) * (size_t)p.Sk * D;
-    const T *Vg = static_cast<const T *>(p.v) + ((size_t)b * p.Hkv + kvh) * (size_t)p.Sk * D;
+    const T *Qg = static_cast<const T *>(p.q) + q_at(p, b, hq, q0);
+    const T *Kg = static_cast<const T *>(p.k) + k_at(p, b, kvh, 0);
+    const T *Vg = static_cast<const T *>(p.v) + v_at(p, b, kvh, 0);
 
     // key range of this split: a fixed partition of [0, Sk) in whole tiles, clipped by causality
     const int n_kt_all = (p.Sk + BN - 1) / BN;
     const int tps = (n_kt_all + p.splits - 1) / p.splits;
     const int k_begin = split * tps * BN;
     int k_end = min(p.Sk, (split + 1) * tps * BN);
-    if (p.causal) k_end = min(k_end, q0 + BM);
+    if (p.causal) k_end = min(k_end, max(k_begin, q0 + BM + p.causal_off));
 
     for (int idx = tid; idx < BM * DP; idx += C::THREADS) {
         const int r = idx / DP, d = idx % DP;
-        Qs[d * C::QS + r] = (q0 + r < p.Sq && d < D) ? ld(Qg + (size_t)r * D + d) : 0.f;
+        Qs[d * C::QS + r] = (q0 + r < p.Sq && d < D) ? ld(Qg + (long long)r * p.q_ss + d) : 0.f;
     }
 
     float m[4], l[4], acc[4][C::OC];
@@ -88,9 +88,8 @@ attn_simt_kernel(const AttnProblem p) {
         for (int idx = tid; idx < BN * DP; idx += C::THREADS) {
             const int c = idx / DP, d = idx % DP;
             const bool ok = (kt0 + c < k_end) && d < D;
-            const size_t off = (size_t)(kt0 + c) * D + d;
-            Ks[d * C::KS + c] = ok ? ld(Kg + off) : 0.f;
-            Vs[c * DP + d] = ok ? ld(Vg + off) : 0.f;
+            Ks[d * C::KS + c] = ok ? ld(Kg + (long long)(kt0 + c) * p.k_ss + d) : 0.f;
+            Vs[c * DP + d] = ok ? ld(Vg + (long long)(kt0 + c) * p.v_ss + d) : 0.f;
         }
         __syncthreads();
 
@@ -120,7 +119,7 @@ attn_simt_kernel(const AttnProblem p) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int key = kt0 + tx * 4 + j;
-                const bool valid = key < k_end && (!p.causal || key <= row);
+                const bool valid = key < k_end && (!p.causal || key <= row + p.causal_off);
                 s[i][j] = valid ? s[i][j] * p.scale_log2 : -INFINITY;
                 tmax = fmaxf(tmax, s[i][j]);
             }
@@ -183,7 +182,7 @@ attn_simt_kernel(const AttnProblem p) {
         const long long row = (long long)bh * p.Sq + r;
         if (p.splits == 1) {
             const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
-            T *Og = static_cast<T *>(p.o) + row * D;
+            T *Og = static_cast<T *>(p.o) + o_at(p, b, hq, r);
 #pragma unroll
             for (int ch = 0; ch < C::NCH; ++ch)
 #pragma unroll
@@ -225,7 +224,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) 
     for (int s = 0; s < p.splits; ++s)
         L += p.part_l[(size_t)s * rows_total + row] * ex2_approx(p.part_m[(size_t)s * rows_total + row] - Mref);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    T *Og = static_cast<T *>(p.o) + row * p.D;
+    const int b = (int)(row / ((long long)p.Hq * p.Sq));
+    const int hq = (int)((row / p.Sq) % p.Hq);
+    T *Og = static_cast<T *>(p.o) + o_at(p, b, hq, row % p.Sq);
     for (int c = lane; c < p.D; c += 32) {
         float a = 0.f;
         for (int s = 0; s < p.splits; ++s) {

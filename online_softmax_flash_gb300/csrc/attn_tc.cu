@@ -92,7 +92,7 @@ __device__ __forceinline__ void settle_copies() {
 
 // One work item: 2 x 128 query rows of one (b, q-head), over the key tiles of this CTA's split.
 struct Item {
-    int q0, bh, kvbh, ntiles, n0, n1, n_kv, kt_begin;
+    int q0, bh, b, hq, kvh, ntiles, n0, n1, n_kv, kt_begin;
 };
 
 // Item of round r for this CTA: rounds walk the item list in snake order (forward on even
@@ -107,18 +107,21 @@ __device__ __forceinline__ bool item_at(const AttnProblem &p, int n_qb, int n_it
     w.bh = (int)(it % units);
     const int qb = p.causal ? (n_qb - 1 - qb_rank) : qb_rank;   // heaviest blocks first
     w.q0 = qb * 2 * BM;
-    const int grp = p.Hq / p.Hkv;
-    w.kvbh = (w.bh / p.Hq) * p.Hkv + (w.bh % p.Hq) / grp;
+    w.b = w.bh / p.Hq;
+    w.hq = w.bh % p.Hq;
+    w.kvh = w.hq / (p.Hq / p.Hkv);
     w.ntiles = (w.q0 + BM < p.Sq) ? 2 : 1;
     const int n_kt_all = (p.Sk + BN - 1) / BN;
     const int tps = (n_kt_all + p.splits - 1) / p.splits;
     w.kt_begin = blockIdx.y * tps;
     const int kt_end = min(n_kt_all, w.kt_begin + tps);
-    // key tiles each Q tile visits (causal: up to the tile's last row)
+    // key tiles each Q tile visits (causal: up to the last key its last row sees)
     int e0 = kt_end, e1 = kt_end;
     if (p.causal) {
-        e0 = min(e0, min(w.q0 + BM - 1, p.Sq - 1) / BN + 1);
-        e1 = min(e1, min(w.q0 + 2 * BM - 1, p.Sq - 1) / BN + 1);
+        const int last0 = min(w.q0 + BM - 1, p.Sq - 1) + p.causal_off;
+        const int last1 = min(w.q0 + 2 * BM - 1, p.Sq - 1) + p.causal_off;
+        e0 = min(e0, last0 < 0 ? 0 : last0 / BN + 1);
+        e1 = min(e1, last1 < 0 ? 0 : last1 / BN + 1);
     }
     w.n0 = max(0, e0 - w.kt_begin);
     w.n1 = w.ntiles == 2 ? max(0, e1 - w.kt_begin) : 0;
@@ -194,7 +197,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 ++qc;
                 mbar_expect_tx(smem_u32(&bars.q_full), w.ntiles * C::TILE);
                 for (int t = 0; t < w.ntiles; ++t)
-                    tma_load_4d<false>(sQ + t * C::TILE, &mq, smem_u32(&bars.q_full), 0, w.q0 + t * BM, 0, w.bh);
+                    tma_load_5d(sQ + t * C::TILE, &mq, smem_u32(&bars.q_full), 0, w.q0 + t * BM, 0, w.hq, w.b);
             }
             for (int j = 0; j < w.n_kv; ++j) {
                 const int n = 2 * (gt + j) + odd;
@@ -202,8 +205,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 ok = mbar_wait(smem_u32(&bars.empty[st]), parity_of(n) ^ 1, &abort_flag);
                 if (!ok) break;
                 mbar_expect_tx(smem_u32(&bars.full[st]), C::TILE);
-                tma_load_4d<false>(sRing + st * C::TILE, map, smem_u32(&bars.full[st]), 0, (w.kt_begin + j) * BN, 0,
-                                   w.kvbh);
+                tma_load_5d(sRing + st * C::TILE, map, smem_u32(&bars.full[st]), 0, (w.kt_begin + j) * BN, 0, w.kvh,
+                            w.b);
             }
             gt += w.n_kv;
         }
@@ -345,12 +348,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
                 tmem_ld_wait();
                 const int key0 = (w.kt_begin + i) * BN;
-                const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > row_first);
+                const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > row_first + p.causal_off);
                 if (need_mask) {
                     // column j of the tile (key key0 + j) is kept iff j < lim: inside the sequence
-                    // and, when causal, not after this row
+                    // and, when causal, not after the last key this row sees
                     int lim = p.Sk - key0;
-                    if (p.causal) lim = min(lim, row - key0 + 1);
+                    if (p.causal) lim = min(lim, row + p.causal_off - key0 + 1);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -373,7 +376,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 const bool rescale = __any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold);
                 float alpha = 1.f;
                 if (rescale) {
-                    alpha = ex2_approx(m_ref - m_new);   // m_ref == -inf -> 0
+                    // the warp rescales together; a row that has seen no key yet (m_new still
+                    // -inf, e.g. all keys of this split are after it) keeps l = 0, not NaN
+                    alpha = ex2_approx(m_ref - (m_new == -INFINITY ? 0.f : m_new));   // m_ref == -inf -> 0
                     l *= alpha;
                     m_ref = m_new;
                 }
@@ -448,9 +453,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 const bool row_ok = row < p.Sq;
                 if (p.splits == 1) {
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + grow * D;
-                    // rows are D * 2 bytes apart, so a 32-byte aligned O gives 32-byte aligned chunks
-                    const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
+                    __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + o_at(p, w.b, w.hq, row);
+                    // 32-byte stores when every row starts on a 32-byte boundary
+                    const bool o32 = ((reinterpret_cast<uintptr_t>(p.o) | (uintptr_t)(p.o_ss * 2) |
+                                       (uintptr_t)(p.o_sh * 2) | (uintptr_t)(p.o_sb * 2)) & 31) == 0;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -521,6 +527,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 }
 
 // ------------------------------------------------------------------------- host side
+// Q, K, V tile maps of a problem (5-D strided views); false when TMA cannot address them.
+bool make_maps(const AttnProblem &p, CUtensorMap *mq, CUtensorMap *mk, CUtensorMap *mv) {
+    return make_bf16_tile_map_strided(mq, p.q, p.D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, BM) &&
+           make_bf16_tile_map_strided(mk, p.k, p.D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) &&
+           make_bf16_tile_map_strided(mv, p.v, p.D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, BN);
+}
+
 template <int D>
 cudaError_t launch_t(const AttnProblem &p, int sm_count, cudaStream_t s) {
     using C = TcCfg<D>;
@@ -532,10 +545,7 @@ cudaError_t launch_t(const AttnProblem &p, int sm_count, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap mq, mk, mv;
-    if (!make_bf16_tile_map(&mq, p.q, D, p.Sq, (long long)p.B * p.Hq, BM) ||
-        !make_bf16_tile_map(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, BN) ||
-        !make_bf16_tile_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, BN))
-        return cudaErrorInvalidValue;
+    if (!make_maps(p, &mq, &mk, &mv)) return cudaErrorInvalidValue;
     const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
     const long long items = (long long)n_qb * p.B * p.Hq;
     if (items >= (1LL << 31)) return cudaErrorInvalidValue;
@@ -557,8 +567,11 @@ long long tc_ctas(const AttnProblem &p) {
 bool attn_tc_supported(const AttnProblem &p, const void *Q, const void *K, const void *V, const void *O) {
     if (p.dtype != OSF_BF16 || p.Sq < 2 || (p.D != 64 && p.D != 128)) return false;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return false;
+    // the epilogue stores 16-byte pieces of each O row
+    if (((p.o_ss | p.o_sh | p.o_sb) * 2) % 16 != 0) return false;
     if (tc_ctas(p) >= (1LL << 31)) return false;
-    return tensor_map_encoder() != nullptr;
+    CUtensorMap mq, mk, mv;
+    return make_maps(p, &mq, &mk, &mv);
 }
 
 int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {

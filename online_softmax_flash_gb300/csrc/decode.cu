@@ -97,7 +97,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
                 if (!ok) break;
                 const uint32_t bar = smem_u32(&full[st]);
                 mbar_expect_tx(bar, C::TILE);
-                tma_load_tile(ring + st * C::TILE, map, bar, (t_begin + i) * KT, kvbh);
+                tma_load_5d(ring + st * C::TILE, map, bar, 0, (t_begin + i) * KT, 0, kvh, b);
                 issued = i + 1;
             }
             if (!ok) {
@@ -114,14 +114,16 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
 
     // ==================================================================== compute warps
     const int r0 = lane >> 2, r1 = r0 + 8, kc = (lane & 3) * 2;
-    const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(p.q) + (size_t)(b * p.Hq + kvh * G) * D;
+    // row g of the 16-row tile is query head kvh * G + g (one query row per head)
+    const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(p.q) + q_at(p, b, kvh * G, 0);
+    const __nv_bfloat16 *Q0 = Qb + (long long)r0 * p.q_sh, *Q1 = Qb + (long long)r1 * p.q_sh;
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        qa[kk][0] = r0 < G ? ld_bf16x2(Qb + r0 * D + kk * 16 + kc) : 0u;
-        qa[kk][1] = r1 < G ? ld_bf16x2(Qb + r1 * D + kk * 16 + kc) : 0u;
-        qa[kk][2] = r0 < G ? ld_bf16x2(Qb + r0 * D + kk * 16 + 8 + kc) : 0u;
-        qa[kk][3] = r1 < G ? ld_bf16x2(Qb + r1 * D + kk * 16 + 8 + kc) : 0u;
+        qa[kk][0] = r0 < G ? ld_bf16x2(Q0 + kk * 16 + kc) : 0u;
+        qa[kk][1] = r1 < G ? ld_bf16x2(Q1 + kk * 16 + kc) : 0u;
+        qa[kk][2] = r0 < G ? ld_bf16x2(Q0 + kk * 16 + 8 + kc) : 0u;
+        qa[kk][3] = r1 < G ? ld_bf16x2(Q1 + kk * 16 + 8 + kc) : 0u;
     }
     float o[C::NT][4];
 #pragma unroll
@@ -240,7 +242,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
         const long long grow = (long long)b * p.Hq + kvh * G + row;
         if (p.splits == 1) {
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            static_cast<__nv_bfloat16 *>(p.o)[grow * D + d] = __float2bfloat16_rn(acc * inv);
+            static_cast<__nv_bfloat16 *>(p.o)[o_at(p, b, kvh * G + row, 0) + d] = __float2bfloat16_rn(acc * inv);
             if (p.lse && d == 0) p.lse[grow] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
         } else {
             p.part_acc[((size_t)split * rows_total + grow) * D + d] = acc;
@@ -250,6 +252,12 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
             }
         }
     }
+}
+
+// K and V tile maps of a problem (5-D strided views); false when TMA cannot address them.
+bool make_maps(const AttnProblem &p, CUtensorMap *mk, CUtensorMap *mv) {
+    return make_bf16_tile_map_strided(mk, p.k, p.D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, KT) &&
+           make_bf16_tile_map_strided(mv, p.v, p.D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, KT);
 }
 
 template <int D>
@@ -262,9 +270,7 @@ cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap mk, mv;
-    if (!make_bf16_tile_map(&mk, p.k, D, p.Sk, (long long)p.B * p.Hkv, KT) ||
-        !make_bf16_tile_map(&mv, p.v, D, p.Sk, (long long)p.B * p.Hkv, KT))
-        return cudaErrorInvalidValue;
+    if (!make_maps(p, &mk, &mv)) return cudaErrorInvalidValue;
     const int n_kt = (p.Sk + KT - 1) / KT;
     const int tps = (n_kt + p.splits - 1) / p.splits;
     dim3 grid((unsigned)(p.B * p.Hkv), (unsigned)p.splits);
@@ -280,8 +286,10 @@ bool decode_supported(const AttnProblem &p, const void *Q, const void *K, const 
     if (p.dtype != OSF_BF16 || p.Sq != 1 || (p.D != 64 && p.D != 128)) return false;
     if (p.Hq / p.Hkv > MAX_G) return false;
     if (!aligned16(K) || !aligned16(V) || (reinterpret_cast<uintptr_t>(Q) & 3u) != 0) return false;
+    if (((p.q_sb | p.q_sh) & 1) != 0) return false;   // Q is read as bf16 pairs
     if ((long long)p.B * p.Hkv >= (1LL << 31)) return false;
-    return tensor_map_encoder() != nullptr;
+    CUtensorMap mk, mv;
+    return make_maps(p, &mk, &mv);
 }
 
 int decode_pick_splits(const AttnProblem &p, int sm_count, int requested) {

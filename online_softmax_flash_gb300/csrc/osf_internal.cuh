@@ -60,13 +60,30 @@ struct AttnProblem {
     float *lse;          // optional [B, Hq, Sq]
     int dtype;           // OSF_F32 / OSF_BF16
     int B, Hq, Hkv, Sq, Sk, D;
-    int causal;          // already folded with Sq > 1
+    int causal;          // 1: key j is visible to query row i iff j <= i + causal_off
+    int causal_off;      // 0 (top-left) or Sk - Sq (bottom-right)
     float scale_log2;    // scale * log2(e)
+    // element strides of the b, h and s dimensions of Q, K, V, O (d is contiguous)
+    long long q_sb, q_sh, q_ss, k_sb, k_sh, k_ss, v_sb, v_sh, v_ss, o_sb, o_sh, o_ss;
     // split-K partial state workspace (float): acc [splits][B*Hq*Sq][D], m/l [splits][B*Hq*Sq]
     int splits;
     float *part_acc, *part_m, *part_l;
     int *status;         // device status word
 };
+
+// Element offsets of row s of head h in batch b.
+__host__ __device__ __forceinline__ long long q_at(const AttnProblem &p, int b, int h, long long s) {
+    return b * p.q_sb + h * p.q_sh + s * p.q_ss;
+}
+__host__ __device__ __forceinline__ long long k_at(const AttnProblem &p, int b, int h, long long s) {
+    return b * p.k_sb + h * p.k_sh + s * p.k_ss;
+}
+__host__ __device__ __forceinline__ long long v_at(const AttnProblem &p, int b, int h, long long s) {
+    return b * p.v_sb + h * p.v_sh + s * p.v_ss;
+}
+__host__ __device__ __forceinline__ long long o_at(const AttnProblem &p, int b, int h, long long s) {
+    return b * p.o_sb + h * p.o_sh + s * p.o_ss;
+}
 
 // Count of kernels launched by the library (diagnostics; see osf_launch_count).
 void count_launches(int n);

@@ -61,6 +61,30 @@ inline bool make_bf16_tile_map(CUtensorMap *m, const void *g, int D, long long Y
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D view (d % 64, s, d / 64, h, b) of a bf16 tensor [B][H][S][D] with element strides sb, sh,
+// ss (d contiguous, D a multiple of 64): one box {64, box_rows, D/64, 1, 1} brings a whole
+// [box_rows x D] tile of one (b, h) in a single TMA instruction, laid out as in
+// make_bf16_tile_map.  TMA needs 16-byte aligned strides (multiples of 8 elements); a
+// dimension of extent 1 takes a placeholder stride.  False when the map cannot be encoded.
+inline bool make_bf16_tile_map_strided(CUtensorMap *m, const void *g, int D, long long S, long long H,
+                                       long long B, long long ss, long long sh, long long sb,
+                                       uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc || D % 64 != 0) return false;
+    auto fix = [](long long extent, long long stride_elems) -> cuuint64_t {
+        return extent > 1 ? (cuuint64_t)stride_elems * 2 : (cuuint64_t)128;
+    };
+    cuuint64_t dims[5] = {64, (cuuint64_t)S, (cuuint64_t)(D / 64), (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[4] = {fix(S, ss), 128, fix(H, sh), fix(B, sb)};
+    for (int i = 0; i < 4; ++i)
+        if (strides[i] == 0 || strides[i] % 16 != 0) return false;
+    cuuint32_t box[5] = {64, box_rows, (cuuint32_t)(D / 64), 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(g), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace osf

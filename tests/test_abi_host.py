@@ -71,6 +71,34 @@ def test_invalid_arguments_rejected_on_host(osf):
     assert lib.osf_attn_workspace_bytes(1, 1, 3, 2, 1, 8, 64, ctypes.byref(n)) == osf.OSF_ERR_INVALID
 
 
+def test_strided_entry_point_rejects_bad_layouts_on_host(osf):
+    """osf_attn_fwd_gqa_ex validates strides and masks before touching the device."""
+    lib = osf.lib()
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 8, 8, 64
+    q, k, v, o = (ctypes.c_void_p(x << 40) for x in (1, 2, 3, 4))
+    bshd_q = [Sq * Hq * D, D, Hq * D]
+    bshd_kv = [Sk * Hkv * D, D, Hkv * D]
+
+    def call(strides, mask=0, out=o, Sq_=Sq, Sk_=Sk):
+        arr = None if strides is None else (ctypes.c_longlong * 12)(*strides)
+        return lib.osf_attn_fwd_gqa_ex(q, k, v, out, osf.OSF_BF16, B, Hq, Hkv, Sq_, Sk_, D,
+                                       None if arr is None else ctypes.cast(arr, ctypes.c_void_p), mask,
+                                       0.0, None, None, 0, None)
+
+    good = bshd_q + bshd_kv + bshd_kv + bshd_q
+    assert call(good, mask=7) == osf.OSF_ERR_INVALID                       # unknown mask
+    assert call(good[:2] + [-Hq * D] + good[3:]) == osf.OSF_ERR_INVALID    # negative stride
+    overlapping_o = good[:9] + [Sq * Hq * D, D, D]                          # rows of O collide
+    assert call(overlapping_o) == osf.OSF_ERR_INVALID
+    broadcast_o = good[:9] + [0, Sq * D, D]                                  # O may not broadcast
+    assert call(broadcast_o) == osf.OSF_ERR_INVALID
+    assert call(good, out=q) == osf.OSF_ERR_INVALID                         # O over Q
+    # inputs may broadcast (stride 0) and any mask is accepted for Sq != Sk; empty problems are no-ops
+    assert call(good, Sq_=0) == osf.OSF_OK
+    assert call(good[:3] + [0, 0, D] + [0, 0, D] + good[9:], Sq_=0) == osf.OSF_OK
+    assert call(good, mask=2, Sk_=0) == osf.OSF_OK
+
+
 def test_binding_refuses_cpu_tensors(osf):
     torch = pytest.importorskip("torch")
     x = torch.zeros(4, 8)
