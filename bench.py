@@ -42,6 +42,14 @@ WORKLOADS = {
     "gqa_causal_prefill": dict(kind="attn", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128, causal=True,
                                dtype="bf16",
                                desc="batched GQA causal prefill B=2 Hq=32 Hkv=8 Sq=Sk=4096 D=128 bf16 [B,H,S,D]"),
+    "gqa_causal_prefill_bshd": dict(kind="attn", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128, causal=True,
+                                    dtype="bf16", layout="bshd",
+                                    desc="batched GQA causal prefill B=2 Hq=32 Hkv=8 Sq=Sk=4096 D=128 bf16 "
+                                         "stored [B,S,H,D], read through strides"),
+    "gqa_chunked_prefill": dict(kind="attn", B=2, Hq=32, Hkv=8, Sq=1024, Sk=4096, D=128, causal=True,
+                                mask="bottom_right", dtype="bf16",
+                                desc="GQA chunked prefill: 1024 new rows after a 3072-key cache (Sk=4096), "
+                                     "bottom-right causal, B=2 Hq=32 Hkv=8 D=128 bf16"),
     "single_head_4096_bf16": dict(kind="attn", B=1, Hq=1, Hkv=1, Sq=4096, Sk=4096, D=64, causal=False,
                                   dtype="bf16", desc="single-head attention M=N=4096 d=64 bf16"),
     "single_head_4096_f32": dict(kind="attn", B=1, Hq=1, Hkv=1, Sq=4096, Sk=4096, D=64, causal=False,
@@ -104,8 +112,13 @@ def work_units(w):
             b = es * (2 * w["B"] * w["Hkv"] * w["Sk"] * w["D"] + 2 * w["B"] * w["Hq"] * w["D"])
             return b / 1e9, "GB/s", "hbm"
         f = 4.0 * w["B"] * w["Hq"] * w["Sq"] * w["Sk"] * w["D"]
-        if w["causal"]:
-            f /= 2
+        if w.get("mask") == "bottom_right":
+            # exactly the visible (row, key) pairs: row i sees min(Sk, i + Sk - Sq + 1) keys
+            off = w["Sk"] - w["Sq"]
+            pairs = sum(max(0, min(w["Sk"], i + off + 1)) for i in range(w["Sq"]))
+            f = 4.0 * w["B"] * w["Hq"] * pairs * w["D"]
+        elif w["causal"]:
+            f /= 2   # the "halved for causal" convention of the headline workload
         return f / 1e12, "TFLOP/s", ("tensor" if w["dtype"] == "bf16" else "alu")
     # softmax: on-chip rows read once and write once; longer rows read twice
     per = 8 if w["T"] <= 32768 else 12
@@ -147,12 +160,16 @@ class Runner:
         import torch
         self.w, self.osf, self.dev = w, osf, dev
         self.host = host
-        self.d_in = [h.to(dev) for h in host]
+        self.bshd = w.get("layout") == "bshd"
+        if self.bshd:   # store [B, S, H, D]; the call reads transposed views through strides
+            self.host = [h.permute(0, 2, 1, 3).contiguous().pin_memory() for h in host]
+        self.d_in = [h.to(dev) for h in self.host]
         if w["kind"] == "solve":
             self.out = torch.empty(w["M"], w["d"], device=dev)
             self.ws = None
         elif w["kind"] == "attn":
             self.out = torch.empty_like(self.d_in[0])
+            self.views = [t.transpose(1, 2) for t in self.d_in + [self.out]] if self.bshd else None
             dt = osf.OSF_BF16 if w["dtype"] == "bf16" else osf.OSF_F32
             n = osf.osf_attn_workspace_bytes(dt, w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Sk"], w["D"])
             self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
@@ -167,6 +184,10 @@ class Runner:
         if w["kind"] == "solve":
             q, k, v = self.d_in
             osf.osf_attn_fwd(q, k, v, self.out, w["M"], w["N"], w["d"])
+        elif w["kind"] == "attn" and (self.bshd or "mask" in w):
+            q, k, v, o = self.views if self.bshd else self.d_in + [self.out]
+            osf.osf_attn_fwd_gqa_ex(q, k, v, out=o, workspace=self.ws,
+                                    mask=w.get("mask", "top_left" if w["causal"] else "none"))
         elif w["kind"] == "attn":
             q, k, v = self.d_in
             osf.osf_attn_fwd_gqa(q, k, v, out=self.out, causal=w["causal"], workspace=self.ws)
@@ -358,8 +379,11 @@ def oracle_timed(name, w, budget_s):
             vv = si.normal_f32((w["Sk"], D), n, si.STREAM_V)
             if w["dtype"] == "bf16":
                 q, kk, vv = (si.bf16_bits_to_f32(si.f32_to_bf16_bits(a)) for a in (q, kk, vv))
+            qi = None
+            if w.get("mask") == "bottom_right":
+                qi = np.arange(S) + (w["Sk"] - S)
             t = time.perf_counter()
-            oracle.attention(q, kk, vv, causal=w["causal"])
+            oracle.attention(q, kk, vv, causal=w["causal"], q_index=qi)
             elapsed += time.perf_counter() - t
             n += 1
             done += per_head
