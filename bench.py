@@ -58,6 +58,10 @@ WORKLOADS = {
                                  desc="single-head attention solve M=64 N=100 d=32 fp32"),
     "gqa_decode": dict(kind="attn", B=8, Hq=32, Hkv=8, Sq=1, Sk=32768, D=128, causal=False, dtype="bf16",
                        desc="GQA decode B=8 Hq=32 Hkv=8 Sq=1 Sk=32768 D=128 bf16, split-K + LSE combine"),
+    "gqa_speculative_decode": dict(kind="attn", B=8, Hq=32, Hkv=8, Sq=4, Sk=32768, D=128, causal=True,
+                                   mask="bottom_right", dtype="bf16",
+                                   desc="GQA speculative decode: 4 draft rows per head against a 32768-key cache, "
+                                        "bottom-right causal, B=8 Hq=32 Hkv=8 D=128 bf16"),
     "softmax_rows": dict(kind="softmax", rows=4096, T=32768,
                          desc="row softmax fp32 [4096, 32768], 8*N(0,1) + one +30 spike per row"),
     "softmax_1d": dict(kind="softmax", rows=1, T=1 << 26,
@@ -107,9 +111,9 @@ def work_units(w):
     if w["kind"] == "solve":
         return 4.0 * w["M"] * w["N"] * w["d"] / 1e12, "TFLOP/s", "alu"
     if w["kind"] == "attn":
-        if w["Sq"] == 1:  # decode: every K/V byte read once, plus Q and O
+        if w["Sq"] * w["Hq"] // w["Hkv"] <= 16:  # decode: every K/V byte read once, plus Q and O
             es = 2 if w["dtype"] == "bf16" else 4
-            b = es * (2 * w["B"] * w["Hkv"] * w["Sk"] * w["D"] + 2 * w["B"] * w["Hq"] * w["D"])
+            b = es * (2 * w["B"] * w["Hkv"] * w["Sk"] * w["D"] + 2 * w["B"] * w["Hq"] * w["Sq"] * w["D"])
             return b / 1e9, "GB/s", "hbm"
         f = 4.0 * w["B"] * w["Hq"] * w["Sq"] * w["Sk"] * w["D"]
         if w.get("mask") == "bottom_right":

@@ -89,9 +89,10 @@ int osf_attn_fwd(const float *Q, const float *K, const float *V, float *out,
  *      osf_attn_workspace_bytes (may be 0, then workspace may be NULL).
  * Sq == 0 or Sk == 0 or B == 0: OSF_OK, nothing written.  Hq % Hkv != 0, causal with
  * Sq > 1 && Sq != Sk, or O overlapping Q/K/V: OSF_ERR_INVALID.  D must be 1..256.
- * Kernel choice (internal): bf16 with D in {64, 128} and Sq > 1 runs the tensor-core
- * (tcgen05/TMEM/TMA) prefill kernel; Sq == 1 runs the split-K decode kernel followed by a
- * log-sum-exp combine; everything else runs the general CUDA-core kernel.
+ * Kernel choice (internal), bf16 with D in {64, 128}: when (Hq / Hkv) * Sq <= 16 (decode,
+ * or a few speculative rows) the split-K decode kernel and a log-sum-exp combine; otherwise
+ * the tensor-core (tcgen05/TMEM/TMA) prefill kernel.  Everything else runs the general
+ * CUDA-core kernel.
  */
 int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int dtype,
                      int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,

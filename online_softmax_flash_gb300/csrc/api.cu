@@ -192,7 +192,9 @@ void carve_partials(AttnProblem &p, void *ws, long long rows) {
 enum class Path { Simt, TensorCore, Decode };
 
 Path choose_path(const AttnProblem &p, const void *Q, const void *K, const void *V, const void *O) {
-    if (p.dtype == OSF_BF16 && p.Sq == 1 && decode_supported(p, Q, K, V, O)) return Path::Decode;
+    // one or a few query rows per head (G * Sq <= 16): the HBM-bound decode kernel, which reads
+    // each K/V byte once for all the query heads of its kv head
+    if (p.dtype == OSF_BF16 && decode_supported(p, Q, K, V, O)) return Path::Decode;
     if (p.dtype == OSF_BF16 && p.Sq > 1 && attn_tc_supported(p, Q, K, V, O)) return Path::TensorCore;
     return Path::Simt;
 }
@@ -297,8 +299,8 @@ int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, 
         const size_t tc = partial_bytes(attn_tc_pick_splits(p, dev->sm_count), (long long)B * Hq * Sq, D);
         if (tc > need) need = tc;
     }
-    if (dtype == OSF_BF16 && Sq == 1) {
-        const size_t dn = partial_bytes(decode_pick_splits(p, dev->sm_count, 0), (long long)B * Hq, D);
+    if (dtype == OSF_BF16 && (long long)(Hq / Hkv) * Sq <= 16) {
+        const size_t dn = partial_bytes(decode_pick_splits(p, dev->sm_count, 0), (long long)B * Hq * Sq, D);
         if (dn > need) need = dn;
     }
     *bytes = need;

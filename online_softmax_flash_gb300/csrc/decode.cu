@@ -1,4 +1,5 @@
-// Split-K decode (one query row per head, Sq == 1) for bfloat16 K/V caches.
+// Split-K decode for bfloat16 K/V caches: one query row per head (Sq == 1), or a few (G * Sq
+// <= 16: speculative decoding, where Sq draft tokens are checked against the cache at once).
 //
 // Decode reads the whole KV cache once per step and does only G = Hq/Hkv query rows of math
 // per kv head, so it is bound by HBM bandwidth.  One CTA takes one (batch, kv head, key chunk):
@@ -14,7 +15,8 @@
 // take 16 keys of every tile and run the recurrence of "softmax_attention", "实现思路" with
 // warp-level tensor-core MMAs (m16n8k16, bf16 in, fp32 accumulate): S = Q K^T with the G query
 // rows padded to 16, then the S accumulator fragments are reused in registers as the P operand
-// of O += P V.  At the end the four warps' states are merged through shared memory.
+// of O += P V.  At the end the four warps' states are merged through shared memory.  With
+// Sq > 1 the 16 rows hold G heads x Sq query rows, each with its own causal key limit.
 #include "decode.cuh"
 #include "sm100_ptx.cuh"
 #include "tma_host.cuh"
@@ -29,7 +31,7 @@ constexpr int NCW = 4;                       // compute warps, 16 keys of each t
 constexpr int NTHREADS = (NCW + 2) * 32;     // + two TMA producer warps (K, V)
 constexpr int STAGES = 3;
 constexpr uint32_t BOXB = 64 * 128;          // one [64 keys x 64 bf16] box, 128-byte rows
-constexpr int MAX_G = 16;                    // query heads per kv head (MMA rows)
+constexpr int MAX_G = 16;                    // query rows per kv head: G * Sq (MMA rows)
 
 template <int D>
 struct DecCfg {
@@ -114,17 +116,23 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
 
     // ==================================================================== compute warps
     const int r0 = lane >> 2, r1 = r0 + 8, kc = (lane & 3) * 2;
-    // row g of the 16-row tile is query head kvh * G + g (one query row per head)
-    const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(p.q) + q_at(p, b, kvh * G, 0);
-    const __nv_bfloat16 *Q0 = Qb + (long long)r0 * p.q_sh, *Q1 = Qb + (long long)r1 * p.q_sh;
+    // row r of the 16-row tile is query row r % Sq of head kvh * G + r / Sq; rows past G * Sq
+    // are zero padding
+    const int R = G * p.Sq;
+    const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *Q0 = Qb + q_at(p, b, kvh * G + r0 / p.Sq, r0 % p.Sq);
+    const __nv_bfloat16 *Q1 = Qb + q_at(p, b, kvh * G + r1 / p.Sq, r1 % p.Sq);
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        qa[kk][0] = r0 < G ? ld_bf16x2(Q0 + kk * 16 + kc) : 0u;
-        qa[kk][1] = r1 < G ? ld_bf16x2(Q1 + kk * 16 + kc) : 0u;
-        qa[kk][2] = r0 < G ? ld_bf16x2(Q0 + kk * 16 + 8 + kc) : 0u;
-        qa[kk][3] = r1 < G ? ld_bf16x2(Q1 + kk * 16 + 8 + kc) : 0u;
+        qa[kk][0] = r0 < R ? ld_bf16x2(Q0 + kk * 16 + kc) : 0u;
+        qa[kk][1] = r1 < R ? ld_bf16x2(Q1 + kk * 16 + kc) : 0u;
+        qa[kk][2] = r0 < R ? ld_bf16x2(Q0 + kk * 16 + 8 + kc) : 0u;
+        qa[kk][3] = r1 < R ? ld_bf16x2(Q1 + kk * 16 + 8 + kc) : 0u;
     }
+    // last key each of this thread's two rows may see (exclusive bound)
+    const int lim0 = p.causal ? min(key_end, r0 % p.Sq + p.causal_off + 1) : key_end;
+    const int lim1 = p.causal ? min(key_end, r1 % p.Sq + p.causal_off + 1) : key_end;
     float o[C::NT][4];
 #pragma unroll
     for (int j = 0; j < C::NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -158,7 +166,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
         for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const bool valid = key_g + n * 8 + (e & 1) < key_end;
+                const bool valid = key_g + n * 8 + (e & 1) < (e < 2 ? lim0 : lim1);
                 s[n][e] = valid ? s[n][e] * sl2 : -INFINITY;
                 if (e < 2) mx0 = fmaxf(mx0, s[n][e]); else mx1 = fmaxf(mx1, s[n][e]);
             }
@@ -225,8 +233,8 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
         *reinterpret_cast<float2 *>(mine + r1 * D + j * 8 + kc) = make_float2(o[j][2], o[j][3]);
     }
     named_barrier(1, NCW * 32);
-    const long long rows_total = (long long)p.B * p.Hq;
-    for (int idx = tid; idx < G * D; idx += NCW * 32) {
+    const long long rows_total = (long long)p.B * p.Hq * p.Sq;
+    for (int idx = tid; idx < R * D; idx += NCW * 32) {
         const int row = idx / D, d = idx % D;
         float M = -INFINITY;
 #pragma unroll
@@ -239,10 +247,11 @@ decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
             acc += wt * sO[(w * MAX_G + row) * D + d];
             L += wt * sm_l[w][row];
         }
-        const long long grow = (long long)b * p.Hq + kvh * G + row;
+        const int hq = kvh * G + row / p.Sq, qi = row % p.Sq;
+        const long long grow = ((long long)b * p.Hq + hq) * p.Sq + qi;
         if (p.splits == 1) {
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            static_cast<__nv_bfloat16 *>(p.o)[o_at(p, b, kvh * G + row, 0) + d] = __float2bfloat16_rn(acc * inv);
+            static_cast<__nv_bfloat16 *>(p.o)[o_at(p, b, hq, qi) + d] = __float2bfloat16_rn(acc * inv);
             if (p.lse && d == 0) p.lse[grow] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
         } else {
             p.part_acc[((size_t)split * rows_total + grow) * D + d] = acc;
@@ -283,10 +292,10 @@ cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
 
 bool decode_supported(const AttnProblem &p, const void *Q, const void *K, const void *V, const void *O) {
     (void)O;
-    if (p.dtype != OSF_BF16 || p.Sq != 1 || (p.D != 64 && p.D != 128)) return false;
-    if (p.Hq / p.Hkv > MAX_G) return false;
+    if (p.dtype != OSF_BF16 || p.Sq < 1 || (p.D != 64 && p.D != 128)) return false;
+    if ((long long)(p.Hq / p.Hkv) * p.Sq > MAX_G) return false;
     if (!aligned16(K) || !aligned16(V) || (reinterpret_cast<uintptr_t>(Q) & 3u) != 0) return false;
-    if (((p.q_sb | p.q_sh) & 1) != 0) return false;   // Q is read as bf16 pairs
+    if (((p.q_sb | p.q_sh | p.q_ss) & 1) != 0) return false;   // Q is read as bf16 pairs
     if ((long long)p.B * p.Hkv >= (1LL << 31)) return false;
     CUtensorMap mk, mv;
     return make_maps(p, &mk, &mv);

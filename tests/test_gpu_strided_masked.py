@@ -122,3 +122,10 @@ def test_bottom_right_rows_without_keys_no_key_split(osf):
     """More work items than SMs (no key split): the first Sq - Sk rows see no key."""
     out, _ = run(osf, 2, 80, 8, 700, 200, 64, "bf16", "bottom_right", layout="bshd", seed=31)
     assert torch.all(out[:, :, :500] == 0)
+
+
+@pytest.mark.parametrize("Sq,mask", [(2, "bottom_right"), (4, "bottom_right"), (3, "top_left"), (4, "none")])
+def test_speculative_rows_on_the_decode_kernel(osf, Sq, mask):
+    """G * Sq <= 16 query rows per kv head (here G = 4): the decode kernel with per-row limits."""
+    run(osf, 2, 16, 4, Sq, 5003, 128, "bf16", mask, layout="bshd", seed=41 + Sq)
+    run(osf, 1, 8, 2, Sq, 700, 64, "bf16", mask, seed=43 + Sq)
