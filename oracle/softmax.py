@@ -30,3 +30,25 @@ def softmax(x) -> np.ndarray:
     with np.errstate(invalid="ignore", divide="ignore"):
         z = e / L
     return np.where(L > 0, z, 0.0)
+
+
+def softmax_masked(x, scale: float = 1.0, causal_period: int = 0) -> np.ndarray:
+    """Row softmax of ``scale * x`` over ``x[rows, T]`` with an optional causal mask, in fp64.
+
+    The softmax of [Q3] "自注意力原理" / "使用triton实现" (a softmax over attention-weight rows
+    with a scale and, for causal attention, the load condition "column <= row", which fills
+    the part above the diagonal with -inf so it becomes 0 after the exponential):
+
+    1. ``s_j = scale * x_j``
+    2. if ``causal_period > 0``: ``s_j = -inf`` for ``j > r % causal_period``, ``r`` the row
+       number -- the row within its own ``[Sq, Sk]`` score matrix when rows of several heads are
+       stacked (``causal_period = Sq``; a single matrix has ``causal_period = rows``)
+    3. :func:`softmax` of ``s``
+    """
+    x = np.asarray(x, dtype=np.float64)
+    s = x * float(scale)
+    if causal_period > 0:
+        rows, T = s.shape
+        r = np.arange(rows) % causal_period
+        s = np.where(np.arange(T)[None, :] > r[:, None], -np.inf, s)
+    return softmax(s)

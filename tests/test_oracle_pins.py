@@ -422,3 +422,34 @@ def test_attention_rows_follows_the_mask():
     o, l = oracle.attention_rows(Q, K, V, rows, mask="bottom_right")
     np.testing.assert_allclose(o, np.stack([full[0, h, i] for _, h, i in rows]), rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(l, np.array([full_lse[0, h, i] for _, h, i in rows]), rtol=1e-13)
+
+
+# --------------------------------------------------------------- scaled / causal row softmax
+def test_softmax_masked_rows_equal_softmax_of_their_prefix():
+    """Each row of the causal softmax is the plain softmax of the columns it keeps (0..r % P),
+    zeros after; the scale multiplies before the max ([Q3] "使用triton实现")."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((10, 7)) * 4
+    for P, scale in ((10, 0.37), (4, 1.0), (0, 2.5)):
+        z = oracle.softmax_masked(x, scale, P)
+        for r in range(10):
+            keep = 7 if P == 0 else min(7, r % P + 1)
+            np.testing.assert_allclose(z[r, :keep], oracle.softmax(scale * x[r, :keep]), rtol=1e-14, atol=0)
+            assert np.all(z[r, keep:] == 0)
+
+
+def test_softmax_masked_defaults_are_the_plain_softmax():
+    x = np.random.default_rng(4).standard_normal((5, 33))
+    assert np.array_equal(oracle.softmax_masked(x), oracle.softmax(x))
+
+
+def test_softmax_masked_brute_force():
+    x = [[0.5, -1.0, 2.0, 0.25], [3.0, 1.0, -2.0, 0.0], [-1.0, -1.0, 4.0, 2.0]]
+    z = oracle.softmax_masked(x, 0.5, 3)
+    for r in range(3):
+        keep = [0.5 * x[r][j] for j in range(4) if j <= r]
+        mx = max(keep)
+        den = sum(math.exp(v - mx) for v in keep)
+        for j in range(4):
+            ref = math.exp(0.5 * x[r][j] - mx) / den if j <= r else 0.0
+            assert abs(z[r][j] - ref) < 1e-15
