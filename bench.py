@@ -66,6 +66,12 @@ WORKLOADS = {
                          desc="row softmax fp32 [4096, 32768], 8*N(0,1) + one +30 spike per row"),
     "softmax_1d": dict(kind="softmax", rows=1, T=1 << 26,
                        desc="1-D softmax fp32 N=2^26, 8*N(0,1) + one +30 spike"),
+    "softmax_rows_bf16": dict(kind="softmax", rows=4096, T=32768, dtype="bf16",
+                              desc="row softmax bf16 in, bf16 out [4096, 32768], 8*N(0,1) + one +30 spike per row"),
+    "softmax_causal_bf16": dict(kind="softmax", rows=8 * 4096, T=4096, dtype="bf16", period=4096,
+                                scale=128 ** -0.5,
+                                desc="causal scaled softmax of attention weights, 8 heads x [4096, 4096] bf16, "
+                                     "scale 128^-0.5 (columns above the diagonal not read)"),
 }
 DEFAULT = "gqa_causal_prefill"
 
@@ -125,6 +131,10 @@ def work_units(w):
             f /= 2   # the "halved for causal" convention of the headline workload
         return f / 1e12, "TFLOP/s", ("tensor" if w["dtype"] == "bf16" else "alu")
     # softmax: on-chip rows read once and write once; longer rows read twice
+    if w.get("dtype") == "bf16":   # bf16 in and out; a causal row reads only its kept columns
+        P, T = w.get("period", 0), w["T"]
+        read = w["rows"] * T if not P else (w["rows"] // P) * sum(min(T, r + 1) for r in range(P))
+        return 2 * (read + w["rows"] * T) / 1e9, "GB/s", "hbm"
     per = 8 if w["T"] <= 32768 else 12
     return per * w["rows"] * w["T"] / 1e9, "GB/s", "hbm"
 
@@ -142,6 +152,8 @@ def make_inputs(name, w, seed=0):
     if w["kind"] == "attn":
         return si.qkv((w["B"], w["Hq"], w["Sq"], w["D"]), (w["B"], w["Hkv"], w["Sk"], w["D"]), seed,
                       dtype=w["dtype"])
+    if w.get("dtype") == "bf16":
+        return (si.f32_to_bf16_bits(si.softmax_rows_input(w["rows"], w["T"], seed)),)
     return (si.softmax_rows_input(w["rows"], w["T"], seed),)
 
 
@@ -179,7 +191,7 @@ class Runner:
             self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
         else:
             self.out = torch.empty_like(self.d_in[0])
-            n = osf.osf_softmax_workspace_bytes(w["rows"], w["T"])
+            n = osf.osf_softmax_ex_workspace_bytes(w["rows"], w["T"])
             self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
 
@@ -196,7 +208,11 @@ class Runner:
             q, k, v = self.d_in
             osf.osf_attn_fwd_gqa(q, k, v, out=self.out, causal=w["causal"], workspace=self.ws)
         else:
-            osf.osf_softmax_rows(self.d_in[0], self.out, workspace=self.ws)
+            if w.get("dtype") == "bf16":
+                osf.osf_softmax_rows_ex(self.d_in[0], self.out, scale=w.get("scale", 1.0),
+                                        causal_period=w.get("period", 0), workspace=self.ws)
+            else:
+                osf.osf_softmax_rows(self.d_in[0], self.out, workspace=self.ws)
 
     def call_e2e(self):
         """Host buffers in, host buffer out: H2D copies, the call, D2H copy of the result."""
@@ -407,11 +423,17 @@ def oracle_timed(name, w, budget_s):
             done += per
         return done / elapsed, unit, f"{n} of {B * Hkv} (b, kv-head) groups", cores
     rows, T = w["rows"], w["T"]
-    step = 64 if rows > 1 else 1
+    P = w.get("period", 0)
+    step = P if P else (64 if rows > 1 else 1)   # whole score matrices keep the causal row numbers
     while n < rows and elapsed < budget_s:
         x = si.softmax_rows_input(step, T, n)
+        if w.get("dtype") == "bf16":
+            x = si.bf16_bits_to_f32(si.f32_to_bf16_bits(x))
         t = time.perf_counter()
-        oracle.softmax(x)
+        if w.get("dtype") == "bf16" or P:
+            oracle.softmax_masked(x, w.get("scale", 1.0), P)
+        else:
+            oracle.softmax(x)
         elapsed += time.perf_counter() - t
         n += step
         done += amount * step / rows

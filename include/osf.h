@@ -188,6 +188,33 @@ int osf_softmax_rows_noalloc(const float *x, float *z, long long rows, long long
                              osf_stream stream);
 
 /*
+ * osf_softmax_rows_ex -- row softmax of scale * x with an optional in-row causal mask, on
+ * float32 or bfloat16 rows with row strides: the softmax of [Q3] "softmax的triton实现", a kernel
+ * over attention-weight rows taking a row stride and a scale, whose causal variant keeps column
+ * <= row (-inf elsewhere, 0 after the exponential); values are widened to float32 on load as
+ * in [SO] "Online Softmax".
+ *     kept(r, j) = (causal_period == 0) || (j <= r % causal_period)
+ *     z[r, j] = kept ? exp(scale*x[r, j] - m_r) / l_r : 0, over the kept columns of row r
+ * x: rows of T elements of x_dtype (OSF_F32 or OSF_BF16), row r at x + r * x_row_stride
+ *    elements; z likewise with z_dtype and z_row_stride.  A stride of 0 means T; strides < T
+ *    -> OSF_ERR_INVALID.  z == x with the same dtype and stride is in place; any other overlap
+ *    -> OSF_ERR_INVALID.
+ * scale: 0 -> 1; NaN or infinite -> OSF_ERR_INVALID.
+ * causal_period: 0 -> no mask; P > 0 -> row r keeps columns 0 .. r % P (stacked [Sq, Sk]
+ *    score matrices use P = Sq; a single matrix P = rows).
+ * workspace: osf_softmax_ex_workspace_bytes(rows, T) bytes (0 for T <= 32768).
+ * Kernel choice: contiguous float32 with scale 1 and no mask runs osf_softmax_rows; rows of up
+ * to 32768 elements with 16-byte aligned starts are held on chip (columns past the causal limit
+ * are not read); others stream through one CTA per row or, beyond 32768, chunks over the GPU.
+ */
+int osf_softmax_rows_ex(const void *x, void *z, int x_dtype, int z_dtype, long long rows, long long T,
+                        long long x_row_stride, long long z_row_stride, float scale, long long causal_period,
+                        void *workspace, size_t workspace_bytes, osf_stream stream);
+
+/* Bytes of workspace osf_softmax_rows_ex needs for [rows, T] (written to *bytes). */
+int osf_softmax_ex_workspace_bytes(long long rows, long long T, size_t *bytes);
+
+/*
  * osf_device_status -- synchronise `stream`, then return (and reset to OSF_OK) the device
  * status word of the current device: OSF_ERR_TIMEOUT if any kernel gave up a bounded wait
  * since the last call, OSF_ERR_CUDA if the synchronisation itself failed, else OSF_OK.

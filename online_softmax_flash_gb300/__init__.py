@@ -17,7 +17,7 @@ __all__ = [
     "osf_status_string", "osf_version", "osf_sm_count", "osf_attn_fwd", "osf_attn_fwd_gqa",
     "osf_attn_workspace_bytes", "osf_attn_decode_gqa", "osf_attn_decode_workspace_bytes",
     "osf_softmax_rows", "osf_softmax_workspace_bytes", "osf_device_status", "osf_launch_count",
-    "solve", "osf_attn_fwd_gqa_ex", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
+    "solve", "osf_attn_fwd_gqa_ex", "osf_softmax_rows_ex", "osf_softmax_ex_workspace_bytes", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
 ]
 
 OSF_OK, OSF_ERR_INVALID, OSF_ERR_UNSUPPORTED, OSF_ERR_CUDA, OSF_ERR_TIMEOUT, OSF_ERR_WORKSPACE = range(6)
@@ -39,6 +39,8 @@ _SIGS = {
     "osf_attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
     "osf_attn_decode_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "osf_softmax_rows": (_i, [_vp, _vp, _ll, _ll, _vp, _sz, _vp]),
+    "osf_softmax_rows_ex": (_i, [_vp, _vp, _i, _i, _ll, _ll, _ll, _ll, _f, _ll, _vp, _sz, _vp]),
+    "osf_softmax_ex_workspace_bytes": (_i, [_ll, _ll, ctypes.POINTER(_sz)]),
     "osf_softmax_workspace_bytes": (_i, [_ll, _ll, ctypes.POINTER(_sz)]),
     "osf_device_status": (_i, [_vp]),
     "osf_launch_count": (ctypes.c_ulonglong, []),
@@ -237,6 +239,36 @@ def osf_softmax_rows(x, z=None, workspace=None):
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().osf_softmax_rows(_ptr(x), _ptr(z), rows, T, _ptr(ws), ws_bytes, _stream(x.device)),
            "osf_softmax_rows")
+    return z
+
+
+def osf_softmax_ex_workspace_bytes(rows: int, T: int) -> int:
+    n = _sz(0)
+    _check(lib().osf_softmax_ex_workspace_bytes(rows, T, ctypes.byref(n)), "osf_softmax_ex_workspace_bytes")
+    return n.value
+
+
+def osf_softmax_rows_ex(x, z=None, out_dtype=None, scale: float = 1.0, causal_period: int = 0, workspace=None):
+    """Row softmax of ``scale * x`` for a float32 or bfloat16 [rows, T] view whose rows may be
+    strided (``x.stride(1) == 1``); ``causal_period`` P > 0 keeps columns ``0 .. r % P`` of row
+    r.  ``z`` (default: a new contiguous tensor of ``out_dtype``, else ``x.dtype``) may be ``x``."""
+    _need_cuda(x, z, contiguous=False)
+    if x.dim() != 2:
+        raise ValueError("osf_softmax_rows_ex takes a 2-D [rows, T] tensor")
+    rows, T = x.shape
+    if z is None:
+        z = torch.empty((rows, T), dtype=out_dtype or x.dtype, device=x.device)
+    for name, t in (("x", x), ("z", z)):
+        if t.shape != (rows, T) or (T > 1 and t.stride(1) != 1):
+            raise ValueError(f"{name} must be [rows, T] with contiguous rows")
+    ws_n = osf_softmax_ex_workspace_bytes(rows, T)
+    ws = _workspace(ws_n, x.device, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    xs = x.stride(0) if rows > 1 else T
+    zs = z.stride(0) if rows > 1 else T
+    _check(lib().osf_softmax_rows_ex(_ptr(x), _ptr(z), _dtype_code(x), _dtype_code(z), rows, T, xs, zs,
+                                     float(scale), int(causal_period), _ptr(ws), ws_bytes, _stream(x.device)),
+           "osf_softmax_rows_ex")
     return z
 
 

@@ -8,6 +8,7 @@
 #include <atomic>
 
 #include "osf_internal.cuh"
+#include "softmax_ex.cuh"
 #include "attn_tc.cuh"
 #include "decode.cuh"
 
@@ -397,6 +398,50 @@ int osf_softmax_rows(const float *x, float *z, long long rows, long long T, void
     if (need > 0 && (!workspace || workspace_bytes < need)) return OSF_ERR_WORKSPACE;
     return launch_status(launch_softmax_rows(x, z, rows, T, static_cast<float *>(workspace),
                                              dev->sm_count, (cudaStream_t)stream));
+}
+
+int osf_softmax_ex_workspace_bytes(long long rows, long long T, size_t *bytes) {
+    if (!bytes) return OSF_ERR_INVALID;
+    *bytes = 0;
+    if (rows < 0 || T < 0) return OSF_ERR_INVALID;
+    if (rows == 0 || T == 0) return OSF_OK;
+    if (rows > 65535 && T > 32768) return OSF_ERR_UNSUPPORTED;
+    DeviceInfo *dev;
+    if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    // the larger of the float32 path's and the general path's needs
+    const size_t a = softmax_workspace_floats(rows, T, dev->sm_count);
+    const size_t b = softmax_ex_workspace_floats(rows, T, dev->sm_count);
+    *bytes = (a > b ? a : b) * sizeof(float);
+    return OSF_OK;
+}
+
+int osf_softmax_rows_ex(const void *x, void *z, int x_dtype, int z_dtype, long long rows, long long T,
+                        long long x_row_stride, long long z_row_stride, float scale, long long causal_period,
+                        void *workspace, size_t workspace_bytes, osf_stream stream) {
+    if ((x_dtype != OSF_F32 && x_dtype != OSF_BF16) || (z_dtype != OSF_F32 && z_dtype != OSF_BF16))
+        return OSF_ERR_INVALID;
+    if (rows < 0 || T < 0 || causal_period < 0 || x_row_stride < 0 || z_row_stride < 0) return OSF_ERR_INVALID;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return OSF_ERR_INVALID;
+    if (rows == 0 || T == 0) return OSF_OK;
+    const long long xs = x_row_stride ? x_row_stride : T, zs = z_row_stride ? z_row_stride : T;
+    if (xs < T || zs < T) return OSF_ERR_INVALID;   // rows may not overlap one another
+    if (!x || !z) return OSF_ERR_INVALID;
+    if (rows > (1LL << 31) - 1 || (rows > 65535 && T > 32768) || xs >= (1LL << 40) || zs >= (1LL << 40))
+        return OSF_ERR_UNSUPPORTED;
+    const size_t nx = (size_t)((rows - 1) * xs + T) * elem_size(x_dtype);
+    const size_t nz = (size_t)((rows - 1) * zs + T) * elem_size(z_dtype);
+    const bool in_place = x == (const void *)z && x_dtype == z_dtype && xs == zs;
+    if (!in_place && overlaps(x, nx, z, nz)) return OSF_ERR_INVALID;
+    const float sc = scale == 0.f ? 1.f : scale;
+    DeviceInfo *dev;
+    if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    if (x_dtype == OSF_F32 && z_dtype == OSF_F32 && sc == 1.f && causal_period == 0 && xs == T && zs == T)
+        return osf_softmax_rows(static_cast<const float *>(x), static_cast<float *>(z), rows, T, workspace,
+                                workspace_bytes, stream);
+    const size_t need = softmax_ex_workspace_floats(rows, T, dev->sm_count) * sizeof(float);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return OSF_ERR_WORKSPACE;
+    SoftmaxExProblem q{x, z, x_dtype, z_dtype, rows, T, xs, zs, sc * kLog2e, causal_period, dev->sm_count};
+    return launch_status(launch_softmax_ex(q, static_cast<float *>(workspace), (cudaStream_t)stream));
 }
 
 int osf_device_status(osf_stream stream) {

@@ -1,0 +1,292 @@
+// Row softmax of scale * x with an optional in-row causal mask, for float32 or bfloat16 rows
+// addressed through row strides: the softmax of "从零开始写Qwen3（五-其一）使用Triton实现自注意力",
+// "softmax的triton实现" (a kernel over attention-weight rows with a row stride, a scale, and the
+// causal variant whose load condition keeps column <= row, filling the rest with -inf), built on
+// the online (m, l) recurrence of "Softmax 算子的实现与优化", "Online Softmax".
+//
+// Column j of row r is kept iff j < lim(r) = min(T, r % P + 1) when the causal period P > 0
+// (stacked [Sq, Sk] score matrices use P = Sq), else lim = T; dropped columns are written as 0.
+// Values are converted to fp32 on load; exponentials are base 2 on x * scale * log2(e).
+//
+// Paths (as for the float32 softmax): a row of up to 32768 elements whose start and stride are
+// 16-byte aligned is held in registers by one CTA (one read, one write per element; columns
+// past lim are not read); other short rows stream twice through one CTA; longer rows are cut
+// into chunks over the whole GPU (chunk states, then merge + normalise).
+#include "osf_internal.cuh"
+#include "softmax_ex.cuh"
+
+namespace osf {
+namespace {
+
+constexpr int kExMaxResidentT = 32768;
+constexpr int kExChunkThreads = 512;
+
+// 16-byte vector loads of E elements, converted to float.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+    static constexpr int E = 4;
+    __device__ __forceinline__ static void load(const float *p, float (&f)[4]) {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int E = 8;
+    __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float (&f)[8]) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(p));
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// Store E floats as E output elements (E * sizeof(Tout) bytes, aligned to that size).
+template <int E> __device__ __forceinline__ void store_vec(float *p, const float (&f)[E]) {
+#pragma unroll
+    for (int i = 0; i < E; i += 4) __stcs(reinterpret_cast<float4 *>(p + i), make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]));
+}
+template <int E> __device__ __forceinline__ void store_vec(__nv_bfloat16 *p, const float (&f)[E]) {
+    uint32_t w[E / 2];
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    if constexpr (E == 8)
+        __stcs(reinterpret_cast<uint4 *>(p), make_uint4(w[0], w[1], w[2], w[3]));
+    else
+        __stcs(reinterpret_cast<uint2 *>(p), make_uint2(w[0], w[1]));
+}
+
+__device__ __forceinline__ float ld1(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float ld1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// CTA-wide merge of per-thread (m, l) states; result broadcast to every thread.
+__device__ __forceinline__ void cta_merge_ml(float &m, float &l, float *sh /* 2*32 */) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+        merge_ml(m, l, m2, l2);
+    }
+    const int W = (blockDim.x + 31) >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (W > 1) {
+        if (lane == 0) { sh[warp] = m; sh[32 + warp] = l; }
+        __syncthreads();
+        m = lane < W ? sh[lane] : -INFINITY;
+        l = lane < W ? sh[32 + lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+            merge_ml(m, l, m2, l2);
+        }
+    }
+}
+
+__device__ __forceinline__ long long row_limit(long long row, long long T, long long period) {
+    return period > 0 ? min(T, row % period + 1) : T;
+}
+
+// One CTA per row; thread t holds vectors t + k * blockDim (k < VPT) of the row in registers.
+template <typename Tin, typename Tout, int VPT>
+__global__ void __launch_bounds__(1024, 1)
+softmax_ex_onchip_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, long long zs, float mult,
+                         long long period) {
+    constexpr int E = Vec<Tin>::E;
+    __shared__ float sh[64];
+    const long long row = blockIdx.x;
+    const Tin *xr = x + row * xs;
+    Tout *zr = z + row * zs;
+    const int nvec = T / E;
+    const int lim = (int)row_limit(row, T, period);
+    float v[VPT][E];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        if (i < nvec && i * E < lim) {
+            Vec<Tin>::load(xr + (long long)i * E, v[k]);
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[k][e] = (i * E + e < lim) ? v[k][e] * mult : -INFINITY;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) m = fmaxf(m, v[k][e]);
+    }
+    const float mref = (m == -INFINITY) ? 0.f : m;
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            v[k][e] = ex2_approx(v[k][e] - mref);
+            l += v[k][e];
+        }
+    float M = m, L = l;
+    cta_merge_ml(M, L, sh);
+    const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - M) / L;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        if (i < nvec) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[k][e] *= f;
+            store_vec<E>(zr + (long long)i * E, v[k]);
+        }
+    }
+}
+
+// (m, l) of the kept columns of x[c0, c1) (values * mult), merged over the CTA.
+template <typename Tin>
+__device__ __forceinline__ void ex_range_state(const Tin *xr, long long c0, long long c1, float mult, float &m,
+                                               float &l, float *sh) {
+    m = -INFINITY;
+    l = 0.f;
+    for (long long i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+        const float a = ld1(xr + i) * mult;
+        const float mn = fmaxf(m, a);
+        const float mr = (mn == -INFINITY) ? 0.f : mn;
+        l = l * ex2_approx(m - mr) + ex2_approx(a - mr);
+        m = mn;
+    }
+    cta_merge_ml(m, l, sh);
+}
+
+// z[c0, c1) = 2^(x * mult - m) / l for kept columns (j < lim), 0 after; from c1 down to c0.
+template <typename Tin, typename Tout>
+__device__ __forceinline__ void ex_range_norm(const Tin *xr, Tout *zr, long long c0, long long c1, long long lim,
+                                              float mult, float m, float l) {
+    const float mref = (m == -INFINITY) ? 0.f : m;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    for (long long i = c1 - 1 - threadIdx.x; i >= c0; i -= blockDim.x)
+        zr[i] = from_f32<Tout>(i < lim ? ex2_approx(ld1(xr + i) * mult - mref) * inv : 0.f);
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kExChunkThreads)
+softmax_ex_stream_kernel(const Tin *x, Tout *z, long long T, long long xs, long long zs, float mult,
+                         long long period) {
+    __shared__ float sh[64];
+    const long long row = blockIdx.x;
+    const long long lim = row_limit(row, T, period);
+    float m, l;
+    ex_range_state(x + row * xs, 0, lim, mult, m, l, sh);
+    ex_range_norm(x + row * xs, z + row * zs, 0, T, lim, mult, m, l);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kExChunkThreads)
+softmax_ex_chunk_state_kernel(const Tin *x, long long T, long long xs, float mult, long long period,
+                              long long chunk, float2 *ws) {
+    __shared__ float sh[64];
+    const long long row = blockIdx.y;
+    const long long lim = row_limit(row, T, period);
+    const long long c0 = (long long)blockIdx.x * chunk;
+    const long long c1 = min(lim, c0 + chunk);
+    float m, l;
+    ex_range_state(x + row * xs, c0, c1, mult, m, l, sh);
+    if (threadIdx.x == 0) ws[row * gridDim.x + blockIdx.x] = make_float2(m, l);
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kExChunkThreads)
+softmax_ex_chunk_norm_kernel(const Tin *x, Tout *z, long long T, long long xs, long long zs, float mult,
+                             long long period, long long chunk, const float2 *__restrict__ ws) {
+    __shared__ float sh[64];
+    const long long row = blockIdx.y;
+    const int nch = gridDim.x;
+    float m = -INFINITY, l = 0.f;
+    for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+        const float2 st = ws[row * nch + c];
+        merge_ml(m, l, st.x, st.y);
+    }
+    cta_merge_ml(m, l, sh);
+    const long long c0 = (long long)blockIdx.x * chunk;
+    const long long c1 = min(T, c0 + chunk);
+    ex_range_norm(x + row * xs, z + row * zs, c0, c1, row_limit(row, T, period), mult, m, l);
+}
+
+bool al16(const void *p, long long stride_bytes) {
+    return ((reinterpret_cast<uintptr_t>(p) | (uintptr_t)stride_bytes) & 15u) == 0;
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_typed(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
+    const Tin *x = static_cast<const Tin *>(q.x);
+    Tout *z = static_cast<Tout *>(q.z);
+    constexpr int E = Vec<Tin>::E;
+    const unsigned rows = (unsigned)q.rows;
+    if (q.T <= kExMaxResidentT && q.T % E == 0 && al16(x, q.xs * (long long)sizeof(Tin)) &&
+        al16(z, q.zs * (long long)sizeof(Tout))) {
+        const int nvec = (int)(q.T / E);
+        int vpt = 1;
+        while (vpt < 32 / E && nvec > 1024 * vpt) vpt *= 2;
+        int threads = (nvec + vpt - 1) / vpt;
+        threads = ((threads + 31) / 32) * 32;
+        const int T = (int)q.T;
+        switch (vpt) {
+            case 1: softmax_ex_onchip_kernel<Tin, Tout, 1><<<rows, threads, 0, s>>>(x, z, T, q.xs, q.zs, q.mult, q.period); break;
+            case 2: softmax_ex_onchip_kernel<Tin, Tout, 2><<<rows, threads, 0, s>>>(x, z, T, q.xs, q.zs, q.mult, q.period); break;
+            case 4: softmax_ex_onchip_kernel<Tin, Tout, 4><<<rows, threads, 0, s>>>(x, z, T, q.xs, q.zs, q.mult, q.period); break;
+            default:
+                if constexpr (E == 4)
+                    softmax_ex_onchip_kernel<Tin, Tout, 8><<<rows, threads, 0, s>>>(x, z, T, q.xs, q.zs, q.mult, q.period);
+                break;
+        }
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    if (q.T <= kExMaxResidentT) {
+        softmax_ex_stream_kernel<Tin, Tout><<<rows, kExChunkThreads, 0, s>>>(x, z, q.T, q.xs, q.zs, q.mult, q.period);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    long long chunk;
+    int nch;
+    softmax_ex_chunk_geometry(q.rows, q.T, q.sm_count, chunk, nch);
+    dim3 grid(nch, rows);
+    float2 *w2 = reinterpret_cast<float2 *>(ws);
+    softmax_ex_chunk_state_kernel<Tin><<<grid, kExChunkThreads, 0, s>>>(x, q.T, q.xs, q.mult, q.period, chunk, w2);
+    softmax_ex_chunk_norm_kernel<Tin, Tout><<<grid, kExChunkThreads, 0, s>>>(x, z, q.T, q.xs, q.zs, q.mult, q.period,
+                                                                             chunk, w2);
+    count_launches(2);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+void softmax_ex_chunk_geometry(long long rows, long long T, int sm_count, long long &chunk, int &nch) {
+    // about four resident CTAs per SM over the whole problem, chunks of at least 8192 elements
+    const long long target_ctas = 4LL * sm_count;
+    long long per_row = (target_ctas + rows - 1) / rows;
+    const long long max_per_row = (T + 8191) / 8192;
+    if (per_row > max_per_row) per_row = max_per_row;
+    if (per_row < 1) per_row = 1;
+    if (per_row > 65535) per_row = 65535;
+    chunk = (T + per_row - 1) / per_row;
+    nch = (int)((T + chunk - 1) / chunk);
+}
+
+size_t softmax_ex_workspace_floats(long long rows, long long T, int sm_count) {
+    if (T <= kExMaxResidentT) return 0;
+    long long chunk;
+    int nch;
+    softmax_ex_chunk_geometry(rows, T, sm_count, chunk, nch);
+    return (size_t)rows * nch * 2;
+}
+
+cudaError_t launch_softmax_ex(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
+    if (q.x_dtype == OSF_F32 && q.z_dtype == OSF_F32) return launch_typed<float, float>(q, ws, s);
+    if (q.x_dtype == OSF_F32) return launch_typed<float, __nv_bfloat16>(q, ws, s);
+    if (q.z_dtype == OSF_F32) return launch_typed<__nv_bfloat16, float>(q, ws, s);
+    return launch_typed<__nv_bfloat16, __nv_bfloat16>(q, ws, s);
+}
+
+}  // namespace osf

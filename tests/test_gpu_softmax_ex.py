@@ -1,0 +1,89 @@
+"""GPU parity of ``osf_softmax_rows_ex`` (scaled, optionally causal row softmax on float32 /
+bfloat16 strided rows) against ``oracle.softmax_masked`` on the same values.
+
+Tolerances: float32 output as for ``osf_softmax_rows`` (max abs 1e-4, row sums 1e-5).  A
+bfloat16 output is the float32 result rounded to nearest bfloat16, which is within 2^-9
+relative; the test allows 4e-3 relative (twice that) and no absolute slack beyond 1e-30.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from conftest import assert_f32_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def to_dev(x32, dtype, pad=0):
+    t = torch.from_numpy(x32).cuda()
+    rows, T = t.shape
+    store = torch.zeros((rows, T + pad), dtype=dtype, device="cuda")
+    store[:, :T] = t.to(dtype)
+    return store[:, :T]
+
+
+def values(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def check(z, ref, what):
+    got = values(z)
+    if z.dtype == torch.bfloat16:
+        err = np.abs(got - ref)
+        bad = err > 4e-3 * np.abs(ref) + 1e-30
+        assert not bad.any(), f"{what}: {bad.sum()} elements off, worst {err.max():.3g}"
+    else:
+        assert_f32_close(got, ref, atol=1e-4, what=what)
+        assert np.abs(got.sum(axis=1) - (ref.sum(axis=1))).max() <= 1e-5, what + " row sums"
+
+
+@pytest.mark.parametrize("T", [1, 7, 8, 100, 1000, 4096, 32768, 40000])
+@pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16")])
+def test_dtypes_and_lengths(osf, T, dtypes):
+    tin, tout = (torch.bfloat16 if d == "bf16" else torch.float32 for d in dtypes)
+    rows = 3 if T > 30000 else 33
+    x32 = si.softmax_rows_input(rows, T, seed=T)
+    x = to_dev(x32, tin)
+    z = osf.osf_softmax_rows_ex(x, out_dtype=tout)
+    check(z, oracle.softmax_masked(values(x)), f"{dtypes} T={T}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("Sq,heads", [(100, 3), (256, 2), (1000, 1)])
+def test_causal_scaled_attention_weights(osf, dtype, Sq, heads):
+    """Stacked [Sq, Sk=Sq] score matrices of several heads: row r keeps columns 0 .. r % Sq."""
+    x32 = (si.normal_f32((heads * Sq, Sq), Sq, si.STREAM_X) * 11).astype(np.float32)
+    x = to_dev(x32, dtype)
+    scale = 64 ** -0.5
+    z = osf.osf_softmax_rows_ex(x, scale=scale, causal_period=Sq)
+    ref = oracle.softmax_masked(values(x), scale, Sq)
+    check(z, ref, f"causal {dtype} Sq={Sq}")
+    got = values(z)
+    assert np.all(got[ref == 0] == 0), "masked columns must be exactly zero"
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_padded_row_strides_and_in_place(osf, dtype):
+    x32 = si.softmax_rows_input(40, 1000, seed=5)
+    x = to_dev(x32, dtype, pad=24)          # row stride 1024: aligned
+    y = to_dev(x32, dtype, pad=3)           # row stride 1003: not 16-byte aligned
+    ref = oracle.softmax_masked(values(x), 0.5, 0)
+    zbuf = torch.full((40, 1000 + 8), 7.0, dtype=dtype, device="cuda")
+    z = osf.osf_softmax_rows_ex(x, zbuf[:, :1000], scale=0.5)
+    check(z, ref, f"strided {dtype}")
+    assert torch.all(zbuf[:, 1000:] == 7.0), "padding of z written"
+    check(osf.osf_softmax_rows_ex(y, scale=0.5), ref, f"unaligned {dtype}")
+    w = osf.osf_softmax_rows_ex(y, y, scale=0.5)   # in place
+    check(w, ref, f"in place {dtype}")
+
+
+def test_bf16_rows_full_size_sampled(osf):
+    """The softmax workload shape (4096 x 32768) in bf16 in and out, checked on sampled rows."""
+    rows, T = 4096, 32768
+    x = torch.from_numpy(si.softmax_rows_input(rows, T, seed=0)).cuda().to(torch.bfloat16)
+    z = osf.osf_softmax_rows_ex(x)
+    pick = [0, 1, 2047, 4095] + list(range(17, rows, 509))
+    check(z[pick], oracle.softmax_masked(values(x[pick])), "bf16 4096x32768 sampled")
