@@ -440,7 +440,8 @@ int osf_softmax_rows_ex(const void *x, void *z, int x_dtype, int z_dtype, long l
                                 workspace_bytes, stream);
     const size_t need = softmax_ex_workspace_floats(rows, T, dev->sm_count) * sizeof(float);
     if (need > 0 && (!workspace || workspace_bytes < need)) return OSF_ERR_WORKSPACE;
-    SoftmaxExProblem q{x, z, x_dtype, z_dtype, rows, T, xs, zs, sc * kLog2e, causal_period, dev->sm_count};
+    SoftmaxExProblem q{x, z, x_dtype, z_dtype, rows, T, xs, zs, sc * kLog2e, causal_period, dev->sm_count,
+                       dev->status};
     return launch_status(launch_softmax_ex(q, static_cast<float *>(workspace), (cudaStream_t)stream));
 }
 

@@ -8,11 +8,16 @@
 // (stacked [Sq, Sk] score matrices use P = Sq), else lim = T; dropped columns are written as 0.
 // Values are converted to fp32 on load; exponentials are base 2 on x * scale * log2(e).
 //
-// Paths (as for the float32 softmax): a row of up to 32768 elements whose start and stride are
-// 16-byte aligned is held in registers by one CTA (one read, one write per element; columns
-// past lim are not read); other short rows stream twice through one CTA; longer rows are cut
-// into chunks over the whole GPU (chunk states, then merge + normalise).
+// Paths: a row of at most 72 KB whose start and stride are 16-byte aligned is staged in shared
+// memory by one bulk copy (up to its causal limit) for a 256-thread CTA, so several rows are in
+// flight per SM and one row's load overlaps the others' arithmetic; other rows of up to 32768
+// elements are held in registers by one CTA of up to 1024 threads (one read, one write per
+// element; columns past lim are not read); unaligned short rows stream twice through one CTA;
+// longer rows are cut into chunks over the whole GPU (chunk states, then merge + normalise).
+#include <mutex>
+
 #include "osf_internal.cuh"
+#include "sm100_ptx.cuh"
 #include "softmax_ex.cuh"
 
 namespace osf {
@@ -25,6 +30,10 @@ constexpr int kExChunkThreads = 512;
 template <typename T> struct Vec;
 template <> struct Vec<float> {
     static constexpr int E = 4;
+    __device__ __forceinline__ static void load_shared(const float *p, float (&f)[4]) {
+        const float4 a = *reinterpret_cast<const float4 *>(p);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    }
     __device__ __forceinline__ static void load(const float *p, float (&f)[4]) {
         const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
         f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
@@ -32,6 +41,15 @@ template <> struct Vec<float> {
 };
 template <> struct Vec<__nv_bfloat16> {
     static constexpr int E = 8;
+    __device__ __forceinline__ static void load_shared(const __nv_bfloat16 *p, float (&f)[8]) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
     __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float (&f)[8]) {
         const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(p));
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
@@ -143,6 +161,78 @@ softmax_ex_onchip_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs
     }
 }
 
+// One CTA of NT threads per row (256; 128 for rows of at most 16 KB and 64 for at most 8 KB,
+// so more rows are in flight per SM); the row (up to its causal limit, rounded up to 16 bytes) is copied into
+// shared memory by one bulk copy, then read twice from there: (m, l), then z.
+constexpr uint32_t kSmemRowBytes = 72 * 1024;
+
+template <typename Tin, typename Tout, int NT>
+__global__ void __launch_bounds__(NT)
+softmax_ex_smem_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, long long zs, float mult,
+                       long long period, int *status) {
+    constexpr int E = Vec<Tin>::E;
+    extern __shared__ __align__(16) uint8_t srow[];
+    __shared__ uint64_t bar;
+    __shared__ float sh[64];
+    const long long row = blockIdx.x;
+    const Tin *xr = x + row * xs;
+    Tout *zr = z + row * zs;
+    const int lim = (int)row_limit(row, T, period);
+    const int nload = (lim + E - 1) / E;                 // 16-byte vectors copied
+    const uint32_t sbuf = ptx::smem_u32(srow);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ptx::mbar_expect_tx(ptx::smem_u32(&bar), (uint32_t)nload * 16u);
+        ptx::bulk_load(sbuf, xr, (uint32_t)nload * 16u, ptx::smem_u32(&bar));
+    }
+    bool ok = ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr);
+    if (!__syncthreads_and(ok)) {
+        // the copy never completed: record it, give it a bounded chance to land, leave
+        if (threadIdx.x == 0) atomicExch(status, kStatusTimeout);
+        ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr, 20000000ull);
+        return;
+    }
+    const Tin *sx = reinterpret_cast<const Tin *>(srow);
+    float m = -INFINITY, l = 0.f;
+    for (int i = threadIdx.x; i < nload; i += NT) {
+        float f[E];
+        Vec<Tin>::load_shared(sx + i * E, f);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            f[e] = (i * E + e < lim) ? f[e] * mult : -INFINITY;
+            mx = fmaxf(mx, f[e]);
+        }
+        const float mn = fmaxf(m, mx);
+        const float mr = (mn == -INFINITY) ? 0.f : mn;
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) s += ex2_approx(f[e] - mr);
+        l = l * ex2_approx(m - mr) + s;
+        m = mn;
+    }
+    cta_merge_ml(m, l, sh);
+    const float mref = (m == -INFINITY) ? 0.f : m;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int nvec = T / E;
+    for (int i = threadIdx.x; i < nvec; i += NT) {
+        float f[E];
+        if (i < nload) {
+            Vec<Tin>::load_shared(sx + i * E, f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[e] = (i * E + e < lim) ? ex2_approx(f[e] * mult - mref) * inv : 0.f;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[e] = 0.f;
+        }
+        store_vec<E>(zr + (long long)i * E, f);
+    }
+}
+
 // (m, l) of the kept columns of x[c0, c1) (values * mult), merged over the CTA.
 template <typename Tin>
 __device__ __forceinline__ void ex_range_state(const Tin *xr, long long c0, long long c1, float mult, float &m,
@@ -223,8 +313,30 @@ cudaError_t launch_typed(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
     Tout *z = static_cast<Tout *>(q.z);
     constexpr int E = Vec<Tin>::E;
     const unsigned rows = (unsigned)q.rows;
-    if (q.T <= kExMaxResidentT && q.T % E == 0 && al16(x, q.xs * (long long)sizeof(Tin)) &&
-        al16(z, q.zs * (long long)sizeof(Tout))) {
+    const bool aligned = q.T % E == 0 && al16(x, q.xs * (long long)sizeof(Tin)) &&
+                         al16(z, q.zs * (long long)sizeof(Tout));
+    if (aligned && (uint64_t)q.T * sizeof(Tin) <= kSmemRowBytes) {
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(softmax_ex_smem_kernel<Tin, Tout, 256>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRowBytes);
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+        const size_t smem = (size_t)q.T * sizeof(Tin);
+        if (smem <= 8 * 1024)
+            softmax_ex_smem_kernel<Tin, Tout, 64><<<rows, 64, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
+                                                                        q.period, q.status);
+        else if (smem <= 16 * 1024)
+            softmax_ex_smem_kernel<Tin, Tout, 128><<<rows, 128, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
+                                                                          q.period, q.status);
+        else
+            softmax_ex_smem_kernel<Tin, Tout, 256><<<rows, 256, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
+                                                                          q.period, q.status);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    if (q.T <= kExMaxResidentT && aligned) {
         const int nvec = (int)(q.T / E);
         int vpt = 1;
         while (vpt < 32 / E && nvec > 1024 * vpt) vpt *= 2;

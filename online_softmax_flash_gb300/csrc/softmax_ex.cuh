@@ -12,6 +12,7 @@ struct SoftmaxExProblem {
     float mult;             // scale * log2(e)
     long long period;       // causal period (0: no mask)
     int sm_count;
+    int *status;            // device status word (bounded-wait expiry)
 };
 void softmax_ex_chunk_geometry(long long rows, long long T, int sm_count, long long &chunk, int &nch);
 size_t softmax_ex_workspace_floats(long long rows, long long T, int sm_count);
