@@ -24,11 +24,13 @@ Every function here is pinned by a ``-m "not gpu"`` test against closed forms, b
 force, worked examples and invariants (``tests/test_oracle_pins.py``).
 """
 from .attention import attention, attention_gqa, attention_rows
+from .attention_bwd import attention_bwd, attention_gqa_bwd
 from .softmax import softmax, softmax_masked
 from .recurrence import (combine_partials, online_attention_row, online_softmax,
                          online_softmax_state)
 
 __all__ = [
-    "attention", "attention_gqa", "attention_rows", "softmax", "softmax_masked",
+    "attention", "attention_gqa", "attention_rows", "attention_bwd", "attention_gqa_bwd", "softmax",
+    "softmax_masked",
     "online_softmax_state", "online_softmax", "online_attention_row", "combine_partials",
 ]

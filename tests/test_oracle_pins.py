@@ -453,3 +453,74 @@ def test_softmax_masked_brute_force():
         for j in range(4):
             ref = math.exp(0.5 * x[r][j] - mx) / den if j <= r else 0.0
             assert abs(z[r][j] - ref) < 1e-15
+
+
+# ------------------------------------------------------------------- backward (gradients)
+def _loss(Q, K, V, dO, mask):
+    O, _ = oracle.attention_gqa(Q, K, V, mask=mask)
+    return float(np.sum(O * dO))
+
+
+@pytest.mark.parametrize("mask", ["none", "top_left", "bottom_right"])
+def test_backward_matches_central_differences(mask):
+    """dQ, dK, dV are the derivatives of L = sum(dO * O) through the forward definition:
+    central differences of the forward oracle, element by element, on a small GQA case."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 3, 5, 3
+    Q = rng.standard_normal((B, Hq, Sq, D)); K = rng.standard_normal((B, Hkv, Sk, D))
+    V = rng.standard_normal((B, Hkv, Sk, D)); dO = rng.standard_normal((B, Hq, Sq, D))
+    grads = oracle.attention_gqa_bwd(Q, K, V, dO, mask=mask)
+    h = 1e-6
+    for t, g in zip((Q, K, V), grads):
+        num = np.zeros_like(t)
+        for idx in np.ndindex(t.shape):
+            keep = t[idx]
+            t[idx] = keep + h; lp = _loss(Q, K, V, dO, mask)
+            t[idx] = keep - h; lm = _loss(Q, K, V, dO, mask)
+            t[idx] = keep
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_backward_single_key_closed_form():
+    """One key: P = 1 whatever Q and K are, so O = V_0, dV_0 = sum_i dO_i, dQ = dK = 0."""
+    rng = np.random.default_rng(12)
+    Q = rng.standard_normal((1, 2, 4, 3)); K = rng.standard_normal((1, 1, 1, 3))
+    V = rng.standard_normal((1, 1, 1, 3)); dO = rng.standard_normal((1, 2, 4, 3))
+    dQ, dK, dV = oracle.attention_gqa_bwd(Q, K, V, dO)
+    assert np.all(dQ == 0) and np.all(dK == 0)
+    np.testing.assert_allclose(dV[0, 0, 0], dO[0].sum(axis=(0, 1)), rtol=1e-14)
+
+
+def test_backward_uniform_attention_closed_form():
+    """Q = 0: every row attends uniformly (P = 1/N).  Then dV_j = sum_i dO_i / N, dK = 0, and
+    dQ_i = scale * sum_j (1/N)(dO_i.V_j - mean_k dO_i.V_k) K_j."""
+    rng = np.random.default_rng(13)
+    M, N, d = 3, 5, 4
+    K = rng.standard_normal((N, d)); V = rng.standard_normal((N, d)); dO = rng.standard_normal((M, d))
+    dQ, dK, dV = oracle.attention_bwd(np.zeros((M, d)), K, V, dO)
+    s = d ** -0.5
+    assert np.allclose(dK, 0, atol=0)
+    for j in range(N):
+        np.testing.assert_allclose(dV[j], dO.sum(axis=0) / N, rtol=1e-14)
+    for i in range(M):
+        a = np.array([dO[i] @ V[j] for j in range(N)])
+        ref = s * sum((a[j] - a.mean()) / N * K[j] for j in range(N))
+        np.testing.assert_allclose(dQ[i], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_backward_gqa_sums_the_heads_of_a_group():
+    """A kv head's dK, dV are the sums of what each of its query heads sends back."""
+    rng = np.random.default_rng(14)
+    Q = rng.standard_normal((2, 4, 5, 3)); K = rng.standard_normal((2, 2, 6, 3))
+    V = rng.standard_normal((2, 2, 6, 3)); dO = rng.standard_normal((2, 4, 5, 3))
+    dQ, dK, dV = oracle.attention_gqa_bwd(Q, K, V, dO, mask="top_left")
+    for b in range(2):
+        for kvh in range(2):
+            sk = np.zeros((6, 3)); sv = np.zeros((6, 3))
+            for hq in (2 * kvh, 2 * kvh + 1):
+                q, k, v = oracle.attention_bwd(Q[b, hq], K[b, kvh], V[b, kvh], dO[b, hq], q_index=np.arange(5))
+                np.testing.assert_allclose(dQ[b, hq], q, rtol=1e-14)
+                sk += k; sv += v
+            np.testing.assert_allclose(dK[b, kvh], sk, rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(dV[b, kvh], sv, rtol=1e-13, atol=1e-15)
