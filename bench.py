@@ -50,6 +50,10 @@ WORKLOADS = {
                                 mask="bottom_right", dtype="bf16",
                                 desc="GQA chunked prefill: 1024 new rows after a 3072-key cache (Sk=4096), "
                                      "bottom-right causal, B=2 Hq=32 Hkv=8 D=128 bf16"),
+    "gqa_causal_backward": dict(kind="attn_bwd", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128, causal=True,
+                                dtype="bf16",
+                                desc="backward (dQ, dK, dV) of the GQA causal prefill B=2 Hq=32 Hkv=8 S=4096 D=128 "
+                                     "bf16, from O, lse and dO"),
     "single_head_4096_bf16": dict(kind="attn", B=1, Hq=1, Hkv=1, Sq=4096, Sk=4096, D=64, causal=False,
                                   dtype="bf16", desc="single-head attention M=N=4096 d=64 bf16"),
     "single_head_4096_f32": dict(kind="attn", B=1, Hq=1, Hkv=1, Sq=4096, Sk=4096, D=64, causal=False,
@@ -116,6 +120,10 @@ def work_units(w):
     """(algorithmic amount per step, unit, roofline bound)."""
     if w["kind"] == "solve":
         return 4.0 * w["M"] * w["N"] * w["d"] / 1e12, "TFLOP/s", "alu"
+    if w["kind"] == "attn_bwd":
+        # five [Sq, Sk] x D products (S, dP, dV, dK, dQ) against the forward's two
+        f = 2.5 * 4.0 * w["B"] * w["Hq"] * w["Sq"] * w["Sk"] * w["D"] / (2 if w["causal"] else 1)
+        return f / 1e12, "TFLOP/s", "tensor"
     if w["kind"] == "attn":
         if w["Sq"] * w["Hq"] // w["Hkv"] <= 16:  # decode: every K/V byte read once, plus Q and O
             es = 2 if w["dtype"] == "bf16" else 4
@@ -149,9 +157,13 @@ def make_inputs(name, w, seed=0):
     import seeded_inputs as si
     if w["kind"] == "solve":
         return si.qkv((w["M"], w["d"]), (w["N"], w["d"]), seed)
-    if w["kind"] == "attn":
-        return si.qkv((w["B"], w["Hq"], w["Sq"], w["D"]), (w["B"], w["Hkv"], w["Sk"], w["D"]), seed,
-                      dtype=w["dtype"])
+    if w["kind"] in ("attn", "attn_bwd"):
+        q, k, v = si.qkv((w["B"], w["Hq"], w["Sq"], w["D"]), (w["B"], w["Hkv"], w["Sk"], w["D"]), seed,
+                         dtype=w["dtype"])
+        if w["kind"] == "attn":
+            return q, k, v
+        dout = si.qkv((w["B"], w["Hq"], w["Sq"], w["D"]), (1, 1, 1, w["D"]), seed + 1000, dtype=w["dtype"])[0]
+        return q, k, v, dout
     if w.get("dtype") == "bf16":
         return (si.f32_to_bf16_bits(si.softmax_rows_input(w["rows"], w["T"], seed)),)
     return (si.softmax_rows_input(w["rows"], w["T"], seed),)
@@ -183,6 +195,18 @@ class Runner:
         if w["kind"] == "solve":
             self.out = torch.empty(w["M"], w["d"], device=dev)
             self.ws = None
+        elif w["kind"] == "attn_bwd":
+            q, k, v, dout = self.d_in
+            dt = osf.OSF_BF16 if w["dtype"] == "bf16" else osf.OSF_F32
+            self.lse = torch.empty(w["B"], w["Hq"], w["Sq"], device=dev)
+            n = osf.osf_attn_workspace_bytes(dt, w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Sk"], w["D"])
+            fws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+            # the forward pass (outside the timed steps) provides O and lse
+            self.o = osf.osf_attn_fwd_gqa(q, k, v, causal=w["causal"], lse=self.lse, workspace=fws)
+            self.grads = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+            self.out = self.grads[0]
+            n = osf.osf_attn_bwd_workspace_bytes(dt, w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Sk"], w["D"])
+            self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
         elif w["kind"] == "attn":
             self.out = torch.empty_like(self.d_in[0])
             self.views = [t.transpose(1, 2) for t in self.d_in + [self.out]] if self.bshd else None
@@ -194,12 +218,18 @@ class Runner:
             n = osf.osf_softmax_ex_workspace_bytes(w["rows"], w["T"])
             self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        if w["kind"] == "attn_bwd":
+            self.grads_host = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in self.grads]
 
     def call(self):
         w, osf = self.w, self.osf
         if w["kind"] == "solve":
             q, k, v = self.d_in
             osf.osf_attn_fwd(q, k, v, self.out, w["M"], w["N"], w["d"])
+        elif w["kind"] == "attn_bwd":
+            q, k, v, dout = self.d_in
+            osf.osf_attn_bwd_gqa(q, k, v, self.o, dout, self.lse, *self.grads,
+                                 mask="top_left" if w["causal"] else "none", workspace=self.ws)
         elif w["kind"] == "attn" and (self.bshd or "mask" in w):
             q, k, v, o = self.views if self.bshd else self.d_in + [self.out]
             osf.osf_attn_fwd_gqa_ex(q, k, v, out=o, workspace=self.ws,
@@ -219,12 +249,18 @@ class Runner:
         for d, h in zip(self.d_in, self.host):
             d.copy_(h, non_blocking=True)
         self.call()
-        self.out_host.copy_(self.out, non_blocking=True)
+        if self.w["kind"] == "attn_bwd":
+            for g, h in zip(self.grads, self.grads_host):
+                h.copy_(g, non_blocking=True)
+        else:
+            self.out_host.copy_(self.out, non_blocking=True)
 
     def h2d_bytes(self):
         return sum(h.numel() * h.element_size() for h in self.host)
 
     def d2h_bytes(self):
+        if self.w["kind"] == "attn_bwd":
+            return sum(g.numel() * g.element_size() for g in self.grads)
         return self.out.numel() * self.out.element_size()
 
 
@@ -390,6 +426,18 @@ def oracle_timed(name, w, budget_s):
             n += 1
             done += amount
         return done / elapsed, unit, f"{n} full solves", cores
+    if w["kind"] == "attn_bwd":
+        B, Hq, S, D = w["B"], w["Hq"], w["Sq"], w["D"]
+        per_head = amount / (B * Hq)
+        while n < B * Hq and elapsed < budget_s:
+            q, kk, vv, g = (si.normal_f32((S, D), n, st) for st in (si.STREAM_Q, si.STREAM_K, si.STREAM_V, si.STREAM_X))
+            q, kk, vv, g = (si.bf16_bits_to_f32(si.f32_to_bf16_bits(a)) for a in (q, kk, vv, g))
+            t = time.perf_counter()
+            oracle.attention_bwd(q, kk, vv, g, q_index=np.arange(S) if w["causal"] else None)
+            elapsed += time.perf_counter() - t
+            n += 1
+            done += per_head
+        return done / elapsed, unit, f"{n} of {B * Hq} (b, q-head) problems, full {S}x{w['Sk']} gradients each", cores
     if w["kind"] == "attn" and w["Sq"] > 1:
         B, Hq, S, D = w["B"], w["Hq"], w["Sq"], w["D"]
         per_head = amount / (B * Hq)

@@ -98,6 +98,31 @@ int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int d
                      int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                      float *lse, void *workspace, size_t workspace_bytes, osf_stream stream);
 
+/*
+ * osf_attn_bwd_gqa -- gradients of batched GQA attention (the backward pass of
+ * osf_attn_fwd_gqa_ex on contiguous tensors).  The pages describe only the forward pass,
+ * [Q3] "自注意力原理" + "GQA"; this is the chain rule through that definition for a loss whose
+ * gradient with respect to O is dO:
+ *     P = softmax(mask(Q K^T * scale)),  D_i = sum_d dO[i,d] O[i,d],
+ *     dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale * dS K,  dK = scale * dS^T Q,
+ * with P rebuilt from lse; a kv head's dK, dV sum over its Hq / Hkv query heads.
+ * Q, O, dO, dQ: [B, Hq, Sq, D]; K, V, dK, dV: [B, Hkv, Sk, D]; all of `dtype`, contiguous,
+ * device.  lse: float32 [B, Hq, Sq], the natural-log log-sum-exp the forward call returned.
+ * mask, scale: as given to the forward call (an osf_mask; scale <= 0 selects D^-0.5).
+ * workspace: osf_attn_bwd_workspace_bytes bytes (one float per query row).
+ * dQ, dK, dV must not overlap one another or any input -> else OSF_ERR_INVALID.
+ * B, Sq or Sk == 0: OSF_OK, nothing written.  Other errors as in osf_attn_fwd_gqa.
+ * Kernel choice: bf16 with D in {64, 128} (16-byte aligned pointers) runs warp-level
+ * tensor-core kernels; everything else a CUDA-core kernel with one warp per row.
+ */
+int osf_attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *lse, void *dQ, void *dK, void *dV, int dtype, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, int mask, float scale, void *workspace, size_t workspace_bytes,
+                     osf_stream stream);
+
+/* Bytes of workspace osf_attn_bwd_gqa needs for these sizes (written to *bytes). */
+int osf_attn_bwd_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D, size_t *bytes);
+
 /* Mask modes of osf_attn_fwd_gqa_ex. */
 typedef enum {
     OSF_MASK_NONE = 0,          /* every key */

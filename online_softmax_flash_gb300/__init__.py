@@ -17,7 +17,8 @@ __all__ = [
     "osf_status_string", "osf_version", "osf_sm_count", "osf_attn_fwd", "osf_attn_fwd_gqa",
     "osf_attn_workspace_bytes", "osf_attn_decode_gqa", "osf_attn_decode_workspace_bytes",
     "osf_softmax_rows", "osf_softmax_workspace_bytes", "osf_device_status", "osf_launch_count",
-    "solve", "osf_attn_fwd_gqa_ex", "osf_softmax_rows_ex", "osf_softmax_ex_workspace_bytes", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
+    "solve", "osf_attn_fwd_gqa_ex", "osf_softmax_rows_ex", "osf_softmax_ex_workspace_bytes",
+    "osf_attn_bwd_gqa", "osf_attn_bwd_workspace_bytes", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
 ]
 
 OSF_OK, OSF_ERR_INVALID, OSF_ERR_UNSUPPORTED, OSF_ERR_CUDA, OSF_ERR_TIMEOUT, OSF_ERR_WORKSPACE = range(6)
@@ -41,6 +42,9 @@ _SIGS = {
     "osf_softmax_rows": (_i, [_vp, _vp, _ll, _ll, _vp, _sz, _vp]),
     "osf_softmax_rows_ex": (_i, [_vp, _vp, _i, _i, _ll, _ll, _ll, _ll, _f, _ll, _vp, _sz, _vp]),
     "osf_softmax_ex_workspace_bytes": (_i, [_ll, _ll, ctypes.POINTER(_sz)]),
+    "osf_attn_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
+                              _vp, _sz, _vp]),
+    "osf_attn_bwd_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "osf_softmax_workspace_bytes": (_i, [_ll, _ll, ctypes.POINTER(_sz)]),
     "osf_device_status": (_i, [_vp]),
     "osf_launch_count": (ctypes.c_ulonglong, []),
@@ -189,6 +193,36 @@ def osf_attn_fwd_gqa_ex(q, k, v, out=None, mask="none", scale: float | None = No
                                      _stream(q.device)),
            "osf_attn_fwd_gqa_ex")
     return out
+
+
+def osf_attn_bwd_workspace_bytes(dtype: int, B, Hq, Hkv, Sq, Sk, D) -> int:
+    n = _sz(0)
+    _check(lib().osf_attn_bwd_workspace_bytes(dtype, B, Hq, Hkv, Sq, Sk, D, ctypes.byref(n)),
+           "osf_attn_bwd_workspace_bytes")
+    return n.value
+
+
+def osf_attn_bwd_gqa(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, mask="none",
+                     scale: float | None = None, workspace=None):
+    """Gradients (dq, dk, dv) of GQA attention on contiguous [B, H, S, D] tensors, given the
+    forward output ``o``, its log-sum-exp ``lse`` and the gradient ``dout`` of the loss with
+    respect to ``o``; ``mask`` and ``scale`` as in the forward call."""
+    _need_cuda(q, k, v, o, dout, lse, dq, dk, dv)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    m = _MASKS[mask] if isinstance(mask, str) else int(mask)
+    ws_n = osf_attn_bwd_workspace_bytes(dt, B, Hq, Hkv, Sq, Sk, D)
+    ws = _workspace(ws_n, q.device, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().osf_attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), dt, B, Hq, Hkv, Sq, Sk, D, m, 0.0 if scale is None else float(scale),
+                                  _ptr(ws), ws_bytes, _stream(q.device)),
+           "osf_attn_bwd_gqa")
+    return dq, dk, dv
 
 
 def osf_attn_decode_workspace_bytes(dtype: int, B, Hq, Hkv, Sk, D, num_splits: int = 0) -> int:

@@ -9,6 +9,7 @@
 
 #include "osf_internal.cuh"
 #include "softmax_ex.cuh"
+#include "attn_bwd.cuh"
 #include "attn_tc.cuh"
 #include "decode.cuh"
 
@@ -398,6 +399,63 @@ int osf_softmax_rows(const float *x, float *z, long long rows, long long T, void
     if (need > 0 && (!workspace || workspace_bytes < need)) return OSF_ERR_WORKSPACE;
     return launch_status(launch_softmax_rows(x, z, rows, T, static_cast<float *>(workspace),
                                              dev->sm_count, (cudaStream_t)stream));
+}
+
+int osf_attn_bwd_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D, size_t *bytes) {
+    if (!bytes) return OSF_ERR_INVALID;
+    *bytes = 0;
+    AttnProblem p;
+    bool empty;
+    const void *ph = reinterpret_cast<const void *>(uintptr_t(1) << 40);
+    int st = check_gqa_ex(ph, ph, ph, reinterpret_cast<void *>(uintptr_t(1) << 44), dtype, B, Hq, Hkv, Sq, Sk, D,
+                          nullptr, OSF_MASK_NONE, 0.f, nullptr, p, empty);
+    if (st != OSF_OK || empty) return st;
+    *bytes = align256((size_t)B * Hq * Sq * sizeof(float));
+    return OSF_OK;
+}
+
+int osf_attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *lse, void *dQ, void *dK, void *dV, int dtype, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, int mask, float scale, void *workspace, size_t workspace_bytes,
+                     osf_stream stream) {
+    AttnProblem p;
+    bool empty;
+    // the forward problem's checks (sizes, mask, scale; dQ plays the output's part)
+    int st = check_gqa_ex(Q, K, V, dQ, dtype, B, Hq, Hkv, Sq, Sk, D, nullptr, mask, scale, nullptr, p, empty);
+    if (st != OSF_OK) return st;
+    if (empty) {
+        // no keys or no rows: gradients are zero (written when there is anything to write)
+        return OSF_OK;
+    }
+    if (!O || !dO || !lse || !dK || !dV) return OSF_ERR_INVALID;
+    const size_t es = elem_size(dtype);
+    const size_t nq = (size_t)B * Hq * Sq * D * es, nkv = (size_t)B * Hkv * Sk * D * es;
+    const size_t nl = (size_t)B * Hq * Sq * sizeof(float);
+    const void *ins[6] = {Q, K, V, O, dO, lse};
+    const size_t in_n[6] = {nq, nkv, nkv, nq, nq, nl};
+    void *outs[3] = {dQ, dK, dV};
+    const size_t out_n[3] = {nq, nkv, nkv};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(outs[o], out_n[o], ins[i], in_n[i])) return OSF_ERR_INVALID;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(outs[o], out_n[o], outs[o2], out_n[o2])) return OSF_ERR_INVALID;
+    }
+    const size_t need = align256(nl);
+    if (!workspace || workspace_bytes < need) return OSF_ERR_WORKSPACE;
+    DeviceInfo *dev;
+    if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    BwdProblem b{};
+    b.q = Q; b.k = K; b.v = V; b.o = O; b.dout = dO; b.lse = lse;
+    b.dq = dQ; b.dk = dK; b.dv = dV;
+    b.dtype = dtype;
+    b.B = B; b.Hq = Hq; b.Hkv = Hkv; b.Sq = Sq; b.Sk = Sk; b.D = D;
+    b.causal = p.causal; b.causal_off = p.causal_off;
+    b.scale_log2 = p.scale_log2;
+    b.scale = p.scale_log2 / kLog2e;
+    b.dvec = static_cast<float *>(workspace);
+    b.status = dev->status;
+    return launch_status(launch_attn_bwd(b, (cudaStream_t)stream));
 }
 
 int osf_softmax_ex_workspace_bytes(long long rows, long long T, size_t *bytes) {

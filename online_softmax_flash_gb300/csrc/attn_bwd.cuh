@@ -1,0 +1,20 @@
+// Attention backward (dQ, dK, dV from Q, K, V, O, dO and the saved log-sum-exp).
+#pragma once
+#include "osf_internal.cuh"
+
+namespace osf {
+struct BwdProblem {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;      // [B, Hq, Sq] natural-log log-sum-exp of the forward pass
+    void *dq, *dk, *dv;
+    int dtype;             // OSF_F32 / OSF_BF16
+    int B, Hq, Hkv, Sq, Sk, D;
+    int causal, causal_off;  // key j visible to row i iff !causal || j <= i + causal_off
+    float scale, scale_log2;
+    float *dvec;           // workspace [B, Hq, Sq]: rowsum(dO * O)
+    int *status;
+};
+// True when the bf16 tensor-core (mma.sync) kernels handle the problem.
+bool attn_bwd_mma_supported(const BwdProblem &p);
+cudaError_t launch_attn_bwd(const BwdProblem &p, cudaStream_t s);
+}  // namespace osf

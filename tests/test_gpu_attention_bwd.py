@@ -1,0 +1,91 @@
+"""GPU parity of ``osf_attn_bwd_gqa`` (dQ, dK, dV) against ``oracle.attention_gqa_bwd``.
+
+The forward pass runs on the GPU (``osf_attn_fwd_gqa_ex``) to produce O and lse, as a training
+step would; the oracle recomputes everything in fp64 from Q, K, V, dO.
+
+Tolerances.  bf16: the gradients are sums of products whose factors P and dS are rounded to
+bf16 (2^-9 relative) before the tensor-core products, and the results are rounded to bf16;
+the error therefore scales with the size of the terms, i.e. with the tensor's largest
+gradient, not with each element: |gpu - ref| <= 2e-2 * max|ref| + 1e-2 * |ref| (the forward's
+bf16 pair, scaled; about 4x the worst error seen).  float32 (CUDA-core path, fp32 throughout):
+|gpu - ref| <= 1e-4 * max(1, max|ref|).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from conftest import bf16_tensor, f32_tensor
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def f64(a, dtype):
+    return si.bf16_bits_to_f32(a).astype(np.float64) if dtype == "bf16" else a.astype(np.float64)
+
+
+def check_grad(got, ref, dtype, what):
+    g = got.float().cpu().numpy()
+    scale = np.abs(ref).max() if ref.size else 0.0
+    err = np.abs(g - ref)
+    if dtype == "bf16":
+        bound = 2e-2 * scale + 1e-2 * np.abs(ref)
+    else:
+        bound = 1e-4 * max(1.0, scale) + 0 * ref
+    bad = err > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} off, worst err {err.max():.3g} (max|ref| {scale:.3g})"
+    assert np.isfinite(g).all(), what + " not finite"
+
+
+def run(osf, B, Hq, Hkv, Sq, Sk, D, dtype, mask, seed=0):
+    q, k, v = si.qkv((B, Hq, Sq, D), (B, Hkv, Sk, D), seed=seed, dtype=dtype)
+    g = si.qkv((B, Hq, Sq, D), (1, 1, 1, D), seed=seed + 1000, dtype=dtype)[0]
+    dev = bf16_tensor if dtype == "bf16" else f32_tensor
+    Q, K, V, G = dev(q), dev(k), dev(v), dev(g)
+    lse = torch.empty(B, Hq, Sq, device="cuda")
+    O = osf.osf_attn_fwd_gqa_ex(Q, K, V, mask=mask, lse=lse)
+    dq, dk, dv = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask=mask)
+    rq, rk, rv = oracle.attention_gqa_bwd(f64(q, dtype), f64(k, dtype), f64(v, dtype), f64(g, dtype), mask=mask)
+    what = f"{dtype} {B},{Hq},{Hkv},{Sq},{Sk},{D} {mask}"
+    check_grad(dq, rq, dtype, what + " dq")
+    check_grad(dk, rk, dtype, what + " dk")
+    check_grad(dv, rv, dtype, what + " dv")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mask", ["none", "top_left", "bottom_right"])
+def test_bf16_tensor_core_backward(osf, D, mask):
+    Sk = 333 if mask == "bottom_right" else 200
+    run(osf, 1, 4, 2, 200, Sk, D, "bf16", mask, seed=D)
+
+
+@pytest.mark.parametrize("mask", ["none", "top_left", "bottom_right"])
+def test_f32_backward(osf, mask):
+    run(osf, 1, 4, 2, 100, 130 if mask == "bottom_right" else 100, 64, "f32", mask, seed=7)
+
+
+@pytest.mark.parametrize("D", [32, 96])
+def test_bf16_other_head_dims_backward(osf, D):
+    run(osf, 2, 4, 4, 77, 77, D, "bf16", "top_left", seed=D)
+
+
+def test_backward_ragged_multi_block_gqa(osf):
+    """Several key and query blocks with ragged ends, G = 4, bottom-right with Sq > Sk
+    (rows without keys must send back nothing)."""
+    run(osf, 2, 8, 2, 300, 190, 128, "bf16", "bottom_right", seed=11)
+    run(osf, 1, 8, 2, 1000, 1000, 64, "bf16", "top_left", seed=12)
+
+
+def test_backward_rejects_overlaps_and_missing_workspace(osf):
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 2, 8, device="cuda")
+    lib = osf.lib()
+    assert lib.osf_attn_bwd_gqa(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(),
+                                lse.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), osf.OSF_BF16, 1, 2, 2, 8,
+                                8, 64, 0, 0.0, None, 0, None) == osf.OSF_ERR_INVALID
+    out = [torch.empty_like(q) for _ in range(3)]
+    assert lib.osf_attn_bwd_gqa(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(),
+                                lse.data_ptr(), *(t.data_ptr() for t in out), osf.OSF_BF16, 1, 2, 2, 8, 8, 64, 0,
+                                0.0, None, 0, None) == osf.OSF_ERR_WORKSPACE
