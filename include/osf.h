@@ -240,6 +240,16 @@ int osf_softmax_rows_ex(const void *x, void *z, int x_dtype, int z_dtype, long l
 int osf_softmax_ex_workspace_bytes(long long rows, long long T, size_t *bytes);
 
 /*
+ * osf_selftest_bounded_wait -- diagnostic of the failure-detection mechanism (the pages have no
+ * counterpart).  Launches one CTA that waits, with the bounded-wait helper every TMA /
+ * tensor-core kernel uses, on an mbarrier nothing arrives on; after limit_ns (1 .. 2e9) the wait
+ * gives up and records OSF_ERR_TIMEOUT in the device status word, which osf_device_status then
+ * returns.  The kernel exits normally: the context stays usable.  limit_ns out of range ->
+ * OSF_ERR_INVALID.
+ */
+int osf_selftest_bounded_wait(unsigned long long limit_ns, osf_stream stream);
+
+/*
  * osf_device_status -- synchronise `stream`, then return (and reset to OSF_OK) the device
  * status word of the current device: OSF_ERR_TIMEOUT if any kernel gave up a bounded wait
  * since the last call, OSF_ERR_CUDA if the synchronisation itself failed, else OSF_OK.

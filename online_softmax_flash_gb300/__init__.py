@@ -18,7 +18,7 @@ __all__ = [
     "osf_attn_workspace_bytes", "osf_attn_decode_gqa", "osf_attn_decode_workspace_bytes",
     "osf_softmax_rows", "osf_softmax_workspace_bytes", "osf_device_status", "osf_launch_count",
     "solve", "osf_attn_fwd_gqa_ex", "osf_softmax_rows_ex", "osf_softmax_ex_workspace_bytes",
-    "osf_attn_bwd_gqa", "osf_attn_bwd_workspace_bytes", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
+    "osf_attn_bwd_gqa", "osf_attn_bwd_workspace_bytes", "osf_selftest_bounded_wait", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
 ]
 
 OSF_OK, OSF_ERR_INVALID, OSF_ERR_UNSUPPORTED, OSF_ERR_CUDA, OSF_ERR_TIMEOUT, OSF_ERR_WORKSPACE = range(6)
@@ -45,6 +45,7 @@ _SIGS = {
     "osf_attn_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                               _vp, _sz, _vp]),
     "osf_attn_bwd_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "osf_selftest_bounded_wait": (_i, [ctypes.c_ulonglong, _vp]),
     "osf_softmax_workspace_bytes": (_i, [_ll, _ll, ctypes.POINTER(_sz)]),
     "osf_device_status": (_i, [_vp]),
     "osf_launch_count": (ctypes.c_ulonglong, []),
@@ -304,6 +305,12 @@ def osf_softmax_rows_ex(x, z=None, out_dtype=None, scale: float = 1.0, causal_pe
                                      float(scale), int(causal_period), _ptr(ws), ws_bytes, _stream(x.device)),
            "osf_softmax_rows_ex")
     return z
+
+
+def osf_selftest_bounded_wait(limit_ns: int = 1_000_000) -> int:
+    """Run the bounded-wait self-test kernel; returns the launch status (the timeout itself is
+    reported by osf_device_status())."""
+    return lib().osf_selftest_bounded_wait(int(limit_ns), _stream(torch.cuda.current_device()))
 
 
 def osf_launch_count() -> int:

@@ -10,6 +10,7 @@
 #include "osf_internal.cuh"
 #include "softmax_ex.cuh"
 #include "attn_bwd.cuh"
+#include "selftest.cuh"
 #include "attn_tc.cuh"
 #include "decode.cuh"
 
@@ -501,6 +502,13 @@ int osf_softmax_rows_ex(const void *x, void *z, int x_dtype, int z_dtype, long l
     SoftmaxExProblem q{x, z, x_dtype, z_dtype, rows, T, xs, zs, sc * kLog2e, causal_period, dev->sm_count,
                        dev->status};
     return launch_status(launch_softmax_ex(q, static_cast<float *>(workspace), (cudaStream_t)stream));
+}
+
+int osf_selftest_bounded_wait(unsigned long long limit_ns, osf_stream stream) {
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return OSF_ERR_INVALID;
+    DeviceInfo *dev;
+    if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    return launch_status(launch_bounded_wait_selftest(limit_ns, dev->status, (cudaStream_t)stream));
 }
 
 int osf_device_status(osf_stream stream) {
