@@ -210,7 +210,10 @@ attn_simt_kernel(const AttnProblem p) {
 }
 
 // Log-sum-exp combine of split partial states: M = max_s m_s, w_s = 2^(m_s - M),
-// O = sum_s w_s acc_s / sum_s w_s l_s, lse = (M + log2 L) ln 2.  One warp per output row.
+// O = sum_s w_s acc_s / sum_s w_s l_s, lse = (M + log2 L) ln 2.  One warp per output row: the
+// lanes first take one split's (m, l) each (M and L by warp reductions), then each lane sums its
+// columns over the splits with the weights broadcast by shuffles; the split loop is unrolled so
+// its loads are in flight together.
 template <typename T>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) {
     const long long rows_total = (long long)p.B * p.Hq * p.Sq;
@@ -218,22 +221,41 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) 
     const int lane = threadIdx.x & 31;
     if (row >= rows_total) return;
     float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.part_m[(size_t)s * rows_total + row]);
+    for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, p.part_m[(size_t)s * rows_total + row]);
+    M = warp_max(M);
     const float Mref = (M == -INFINITY) ? 0.f : M;
     float L = 0.f;
-    for (int s = 0; s < p.splits; ++s)
+    for (int s = lane; s < p.splits; s += 32)
         L += p.part_l[(size_t)s * rows_total + row] * ex2_approx(p.part_m[(size_t)s * rows_total + row] - Mref);
+    L = warp_sum(L);
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int b = (int)(row / ((long long)p.Hq * p.Sq));
     const int hq = (int)((row / p.Sq) % p.Hq);
     T *Og = static_cast<T *>(p.o) + o_at(p, b, hq, row % p.Sq);
-    for (int c = lane; c < p.D; c += 32) {
-        float a = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-            const float w = ex2_approx(p.part_m[(size_t)s * rows_total + row] - Mref);
-            a += w * p.part_acc[((size_t)s * rows_total + row) * p.D + c];
+    constexpr int CMAX = 8;   // columns per lane (D <= 256)
+    float a[CMAX];
+#pragma unroll
+    for (int k = 0; k < CMAX; ++k) a[k] = 0.f;
+    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+        // this lane's weight for split s0 + lane
+        const int sl = s0 + lane;
+        const float wl = sl < p.splits ? ex2_approx(p.part_m[(size_t)sl * rows_total + row] - Mref) : 0.f;
+        const int n = min(32, p.splits - s0);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, j);
+            const float *acc = p.part_acc + ((size_t)(s0 + j) * rows_total + row) * p.D;
+#pragma unroll
+            for (int k = 0; k < CMAX; ++k) {
+                const int c = lane + 32 * k;
+                if (c < p.D) a[k] += w * acc[c];
+            }
         }
-        Og[c] = from_f32<T>(a * inv);
+    }
+#pragma unroll
+    for (int k = 0; k < CMAX; ++k) {
+        const int c = lane + 32 * k;
+        if (c < p.D) Og[c] = from_f32<T>(a[k] * inv);
     }
     if (p.lse && lane == 0) p.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
