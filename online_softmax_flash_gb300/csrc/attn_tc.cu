@@ -570,8 +570,10 @@ bool attn_tc_supported(const AttnProblem &p, const void *Q, const void *K, const
     // the epilogue stores 16-byte pieces of each O row
     if (((p.o_ss | p.o_sh | p.o_sb) * 2) % 16 != 0) return false;
     if (tc_ctas(p) >= (1LL << 31)) return false;
-    CUtensorMap mq, mk, mv;
-    return make_maps(p, &mq, &mk, &mv);
+    return tensor_map_encoder() != nullptr &&
+           tile_map_addressable(p.q, p.D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb) &&
+           tile_map_addressable(p.k, p.D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb) &&
+           tile_map_addressable(p.v, p.D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb);
 }
 
 int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {

@@ -297,8 +297,9 @@ bool decode_supported(const AttnProblem &p, const void *Q, const void *K, const 
     if (!aligned16(K) || !aligned16(V) || (reinterpret_cast<uintptr_t>(Q) & 3u) != 0) return false;
     if (((p.q_sb | p.q_sh | p.q_ss) & 1) != 0) return false;   // Q is read as bf16 pairs
     if ((long long)p.B * p.Hkv >= (1LL << 31)) return false;
-    CUtensorMap mk, mv;
-    return make_maps(p, &mk, &mv);
+    return tensor_map_encoder() != nullptr &&
+           tile_map_addressable(p.k, p.D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb) &&
+           tile_map_addressable(p.v, p.D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb);
 }
 
 int decode_pick_splits(const AttnProblem &p, int sm_count, int requested) {

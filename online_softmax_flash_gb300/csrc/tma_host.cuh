@@ -85,6 +85,18 @@ inline bool make_bf16_tile_map_strided(CUtensorMap *m, const void *g, int D, lon
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// True when make_bf16_tile_map_strided can describe the tensor (no encoding call): 16-byte
+// aligned base, D a multiple of 64, and every stride of a dimension longer than one a non-zero
+// multiple of 16 bytes below 2^40.
+inline bool tile_map_addressable(const void *g, int D, long long S, long long H, long long B, long long ss,
+                                 long long sh, long long sb) {
+    if ((reinterpret_cast<uintptr_t>(g) & 15u) != 0 || D % 64 != 0) return false;
+    const long long ext[3] = {S, H, B}, st[3] = {ss, sh, sb};
+    for (int i = 0; i < 3; ++i)
+        if (ext[i] > 1 && (st[i] <= 0 || (st[i] * 2) % 16 != 0 || st[i] * 2 >= (1LL << 40))) return false;
+    return true;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace osf
