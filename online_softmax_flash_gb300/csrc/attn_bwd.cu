@@ -14,10 +14,13 @@
 // blocks its rows see.  bf16 with D in {64, 128} runs (2) and (3) on warp-level tensor cores
 // (mma.sync m16n8k16, bf16 in, fp32 accumulate): each warp owns 16 rows, the score
 // accumulators are reused in registers as the A operand of the next product (as in the decode
-// kernel); other problems run a CUDA-core version with one warp per output row.
+// kernel); other problems run a CUDA-core version with one warp per output row.  bf16 with D in
+// {64, 128} and aligned pointers normally takes the tcgen05 kernels of attn_bwd_tc.cu instead;
+// the warp-level kernels remain for pointers TMA cannot address.
 #include <mutex>
 
 #include "attn_bwd.cuh"
+#include "attn_bwd_tc.cuh"
 #include "sm100_ptx.cuh"
 
 namespace osf {
@@ -496,6 +499,7 @@ cudaError_t launch_attn_bwd(const BwdProblem &p, cudaStream_t s) {
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (attn_bwd_tc_supported(p)) return launch_attn_bwd_tc(p, s);
     if (attn_bwd_mma_supported(p)) return p.D == 64 ? launch_mma<64>(p, s) : launch_mma<128>(p, s);
     return p.dtype == OSF_BF16 ? launch_simt<__nv_bfloat16>(p, s) : launch_simt<float>(p, s);
 }
