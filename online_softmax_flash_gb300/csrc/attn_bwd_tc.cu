@@ -3,19 +3,30 @@
 // from the forward's log-sum-exp), with every product a tcgen05.mma into TMEM and the operand
 // tiles streamed by TMA, as in the forward kernel.
 //
-// dQ kernel: one CTA per (b, q head, 128 query rows).  Warp 0 loads Q and dO once and streams
-// K, V tiles (128 keys) through a ring; warp 1 issues S = Q K^T and dP = dO V^T (both operands in
-// shared memory) into TMEM, then dQ += dS K with dS read from TMEM; warps 4-7 (thread r = row r)
-// rebuild P, form dS = P (dP - D_r) and write it as bf16 over S.
+// Warp roles (384 threads): warp 0 issues the TMA loads, warp 1 the MMAs, warp 2 (dK/dV kernel)
+// fills a small ring of per-query lse / D tables, warps 4-11 compute.  Compute warp w owns the
+// TMEM lanes 32 (w % 4) .. +31 (one row of the tile per thread) and one half of the 128 columns,
+// h = (w - 4) / 4, so two warps share each sub-partition.
 //
-// dK/dV kernel: one CTA per (b, kv head, 128 keys) walks every query head of the group and every
-// query tile that sees these keys: S^T = K Q^T, dP^T = V dO^T, then dV += P^T dO and
-// dK += dS^T Q with P^T and dS^T read from TMEM; thread r owns key r, so each column (query) of
-// P^T needs that query's lse and D, read from a small shared-memory table per tile.
+// Each step works in two phases that let the tensor pipe run ahead of the compute warps:
+//   phase A reads the scores, rebuilds P (kept in fp32 registers) and releases the score
+//   columns; phase B reads dP and forms dS = P (dP - D).
 //
-// TMEM (dQ): S [0,128), dP [128,256), dQ [256,256+D).  (dK/dV): S^T [0,128), dP^T [128,256),
-// dK [256,256+D), dV [256+D,256+2D).  bf16 P / dS overwrite the first 64 columns of their region.
+// dK/dV kernel: one CTA per (b, kv head, 128 keys), K and V resident, walking every query tile
+// of every query head of the group that sees these keys.  Per step j (query tile Q_j, dO_j):
+//   S^T = K Q_j^T, dP^T = V dO_j^T;  A: P^T as bf16 over the first half of each warp's S^T
+//   columns, then dV += P^T dO_j;  B: dS^T over dP^T, then dK += dS^T Q_j.
+//   Pipe order: dV_j, S^T_{j+1} (while phase B runs), dK_j, dP^T_{j+1} (while phase A of j+1 runs).
+// dQ kernel: one CTA per (b, q head, 128 query rows), Q and dO resident, K_j, V_j streamed:
+//   S = Q K_j^T, dP = dO V_j^T;  A releases S (S_{j+1} is issued at once);  B writes dS as bf16
+//   into its own columns, then dQ += dS K_j and dP_{j+1}.
+//
+// TMEM (512 columns).  dK/dV: S^T [0,128), dP^T [128,256), dK [256,256+D), dV [256+D,256+2D).
+// dQ: S [0,128), dP [128,256), dQ [256,256+D), dS (bf16) [256+D,256+D+64).
 // Every wait is bounded (2 s): on expiry the CTA records OSF_ERR_TIMEOUT, drains, frees TMEM.
+// TMEM loads and stores are warp-collective: every lane of a warp issues them, and only the
+// global stores of rows outside the problem are skipped.
+#include <climits>
 #include <mutex>
 
 #include "attn_bwd.cuh"
@@ -29,21 +40,22 @@ namespace {
 using namespace ptx;
 
 constexpr int TB = 128;                 // rows (queries or keys) per tile
-constexpr int NT_THREADS = 256;         // warp 0 TMA, warp 1 MMA, warps 4-7 compute
+constexpr int NT_THREADS = 384;         // warps 0-3 control, 4-11 compute
+constexpr int NCW = 8;                  // compute warps
 constexpr int MAX_RING = 8;
+constexpr int TSTAGES = 4;              // lse / D table stages (dK/dV kernel)
 constexpr uint32_t TMEM_COLS = 512;
 
 template <int D>
 struct BtCfg {
-    // ring stages of one [128 x D] bf16 tile each; at D = 64 the deeper ring also keeps one CTA
-    // per SM, so the CTAs do not queue for TMEM (each takes all 512 columns)
+    // ring stages of one [128 x D] bf16 tile each
     static constexpr int RING = D == 64 ? 8 : 4;
     static constexpr uint32_t TILE = TB * D * 2;
     static constexpr uint32_t DBLK = TB * 128;                  // bytes between 64-column blocks
     static constexpr uint32_t A_OFF = 0;                        // two resident tiles (Q, dO) or (K, V)
     static constexpr uint32_t RING_OFF = 2 * TILE;
-    static constexpr uint32_t TAB_OFF = RING_OFF + RING * TILE;  // lse / D tables (dK/dV kernel)
-    static constexpr uint32_t SMEM_BYTES = TAB_OFF + 4 * TB * 4 + 1024;
+    static constexpr uint32_t TAB_OFF = RING_OFF + RING * TILE;  // [TSTAGES][2][128] floats
+    static constexpr uint32_t SMEM_BYTES = TAB_OFF + TSTAGES * 2 * TB * 4 + 1024;
     static constexpr uint32_t IDESC_SS = idesc_bf16_f32(TB, TB, 0, 0);   // [128 x 128] scores
     static constexpr uint32_t IDESC_TS = idesc_bf16_f32(TB, D, 0, 1);    // [128 x D] += P [128 x 128] X
 };
@@ -51,7 +63,8 @@ struct BtCfg {
 struct BtBars {
     uint64_t a_full;
     uint64_t full[MAX_RING], empty[MAX_RING];
-    uint64_t s_full, p_full, done, drain;
+    uint64_t t_full[TSTAGES], t_empty[TSTAGES];
+    uint64_t s_full, dp_full, pa, pb, done, drain;
 };
 
 __device__ __forceinline__ void bt_timeout(volatile int *abort, int *status) {
@@ -65,12 +78,14 @@ __device__ __forceinline__ void bt_settle() {
 }
 
 // X (+)= A(tmem, bf16 [128 x 128]) * B(smem tile [128 x D], MN-major): 8 k-steps of 16 rows.
+// A's k-steps 0-3 start at column `a_lo`, 4-7 at `a_hi` (two warps write the two halves).
 template <int D>
-__device__ __forceinline__ void issue_ts(uint32_t dst, uint32_t a_tmem, uint32_t b_tile, bool acc) {
+__device__ __forceinline__ void issue_ts(uint32_t dst, uint32_t a_lo, uint32_t a_hi, uint32_t b_tile, bool acc) {
     using C = BtCfg<D>;
     const uint64_t bd = sdesc_sw128(b_tile, C::DBLK, 1024);
 #pragma unroll
-    for (int k = 0; k < TB / 16; ++k) mma_ts(dst, a_tmem + k * 8, bd + ((k * 2048) >> 4), C::IDESC_TS, acc || k > 0);
+    for (int k = 0; k < TB / 16; ++k)
+        mma_ts(dst, (k < 4 ? a_lo : a_hi - 32) + k * 8, bd + ((k * 2048) >> 4), C::IDESC_TS, acc || k > 0);
 }
 // X = A(smem tile [128 x D]) * B(smem tile [128 x D])^T: D/16 k-steps.
 template <int D>
@@ -82,6 +97,54 @@ __device__ __forceinline__ void issue_ss(uint32_t dst, uint32_t a_tile, uint32_t
         const uint32_t off = ((k >> 2) * C::DBLK + (k & 3) * 32) >> 4;
         mma_ss(dst, ad + off, bd + off, C::IDESC_SS, k > 0);
     }
+}
+
+__device__ __forceinline__ void pack_store16(uint32_t taddr, const float (&v)[32]) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+    tmem_st16(taddr, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7], pk[8], pk[9], pk[10], pk[11], pk[12],
+              pk[13], pk[14], pk[15]);
+}
+
+// 32 columns of TMEM (fp32) times `sc`, as bf16, to global memory when `store`.
+__device__ __forceinline__ void tmem_to_bf16(uint32_t taddr, bool have, float sc, bool store, __nv_bfloat16 *dst) {
+    uint32_t o[32];
+    if (have) {
+        tmem_ld32(taddr, o);
+        tmem_ld_wait();
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        pk[k] = have ? pack_bf16x2(__uint_as_float(o[2 * k]) * sc, __uint_as_float(o[2 * k + 1]) * sc) : 0u;
+    if (store) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void init_bars(BtBars &bars, volatile int &abort_flag) {
+    using C = BtCfg<D>;
+    mbar_init(smem_u32(&bars.a_full), 1);
+    for (int s = 0; s < C::RING; ++s) {
+        mbar_init(smem_u32(&bars.full[s]), 1);
+        mbar_init(smem_u32(&bars.empty[s]), 1);
+    }
+    for (int s = 0; s < TSTAGES; ++s) {
+        mbar_init(smem_u32(&bars.t_full[s]), 32);
+        mbar_init(smem_u32(&bars.t_empty[s]), NCW);
+    }
+    mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.dp_full), 1);
+    mbar_init(smem_u32(&bars.pa), NCW);
+    mbar_init(smem_u32(&bars.pb), NCW);
+    mbar_init(smem_u32(&bars.done), 1);
+    mbar_init(smem_u32(&bars.drain), 1);
+    abort_flag = 0;
+    mbar_init_fence();
 }
 
 // ====================================================================== dQ
@@ -97,8 +160,10 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + C::A_OFF, sG = sQ + C::TILE, sRing = sbase + C::RING_OFF;
-    const int q0 = blockIdx.x * TB;
-    const int bh = blockIdx.y, b = bh / p.Hq, hq = bh % p.Hq;
+    // the query tiles that see the most key tiles (the last ones, under a causal mask) go first
+    const int BH = p.B * p.Hq, nqt = (p.Sq + TB - 1) / TB;
+    const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * TB;
+    const int bh = blockIdx.x % BH, b = bh / p.Hq, hq = bh % p.Hq;
     const int kvh = hq / (p.Hq / p.Hkv);
     int n = (p.Sk + TB - 1) / TB;   // key tiles these rows see
     if (p.causal) {
@@ -106,24 +171,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         n = min(n, last < 0 ? 0 : last / TB + 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_sh), TMEM_COLS);
-    if (tid == 32) {
-        mbar_init(smem_u32(&bars.a_full), 1);
-        for (int s = 0; s < C::RING; ++s) {
-            mbar_init(smem_u32(&bars.full[s]), 1);
-            mbar_init(smem_u32(&bars.empty[s]), 1);
-        }
-        mbar_init(smem_u32(&bars.s_full), 1);
-        mbar_init(smem_u32(&bars.p_full), 4);
-        mbar_init(smem_u32(&bars.done), 1);
-        mbar_init(smem_u32(&bars.drain), 1);
-        abort_flag = 0;
-        mbar_init_fence();
-    }
+    if (tid == 32) init_bars<D>(bars, abort_flag);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_sh;
-    const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+    const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256, tdS = tmem + 256 + D;
 
     if (warp == 0 && lane == 0 && n > 0) {
         // ------------------------------------------------------------ TMA: Q, dO; then K_j V_j
@@ -148,29 +201,44 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         auto wait_full = [&](int m) {
             return mbar_wait_spin(smem_u32(&bars.full[m % C::RING]), (m / C::RING) & 1, &abort_flag);
         };
-        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag);
-        if (ok) ok = wait_full(0) && wait_full(1);
+        auto ring = [&](int m) { return sRing + (m % C::RING) * C::TILE; };
+        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag) && wait_full(0);
         if (ok) {
             tc_fence_after();
-            issue_ss<D>(tS, sQ, sRing + 0 * C::TILE);          // S = Q K_0^T
-            issue_ss<D>(tP, sG, sRing + 1 * C::TILE);          // dP = dO V_0^T
+            issue_ss<D>(tS, sQ, ring(0));                      // S = Q K_0^T
             mma_commit(smem_u32(&bars.s_full));
-            mma_commit(smem_u32(&bars.empty[1 % C::RING]));       // V_0 is done
+            ok = wait_full(1);
+        }
+        if (ok) {
+            tc_fence_after();
+            issue_ss<D>(tP, sG, ring(1));                      // dP = dO V_0^T
+            mma_commit(smem_u32(&bars.dp_full));
+            mma_commit(smem_u32(&bars.empty[1 % C::RING]));     // V_0 is done
         }
         for (int j = 0; j < n && ok; ++j) {
             const int mk_ = 2 * j;
-            ok = mbar_wait_spin(smem_u32(&bars.p_full), j & 1, &abort_flag);
+            // phase A of step j has read S: the next S may overwrite it
+            ok = mbar_wait_spin(smem_u32(&bars.pa), j & 1, &abort_flag);
             if (!ok) break;
-            tc_fence_after();
-            issue_ts<D>(tQ, tS, sRing + (mk_ % C::RING) * C::TILE, j > 0);   // dQ += dS K_j
-            mma_commit(smem_u32(&bars.empty[mk_ % C::RING]));                // K_j is done
             if (j + 1 < n) {
-                ok = wait_full(mk_ + 2) && wait_full(mk_ + 3);
+                ok = wait_full(mk_ + 2);
                 if (!ok) break;
                 tc_fence_after();
-                issue_ss<D>(tS, sQ, sRing + ((mk_ + 2) % C::RING) * C::TILE);
-                issue_ss<D>(tP, sG, sRing + ((mk_ + 3) % C::RING) * C::TILE);
+                issue_ss<D>(tS, sQ, ring(mk_ + 2));
                 mma_commit(smem_u32(&bars.s_full));
+            }
+            // phase B has read dP and written dS
+            ok = mbar_wait_spin(smem_u32(&bars.pb), j & 1, &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_ts<D>(tQ, tdS, tdS + 32, ring(mk_), j > 0);   // dQ += dS K_j
+            mma_commit(smem_u32(&bars.empty[mk_ % C::RING]));   // K_j is done
+            if (j + 1 < n) {
+                ok = wait_full(mk_ + 3);
+                if (!ok) break;
+                tc_fence_after();
+                issue_ss<D>(tP, sG, ring(mk_ + 3));
+                mma_commit(smem_u32(&bars.dp_full));
                 mma_commit(smem_u32(&bars.empty[(mk_ + 3) % C::RING]));
             }
         }
@@ -180,13 +248,15 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ compute: dS, then dQ out
-        const int r = tid - 128, row = q0 + r;
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int q4 = warp & 3, h = (warp - 4) >> 2;
+        const int r = q4 * 32 + lane, row = q0 + r;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool row_ok = row < p.Sq;
         const long long grow = (long long)bh * p.Sq + row;
         const float lse2 = row_ok ? p.lse[grow] * kLog2e : INFINITY;
         const float dvr = row_ok ? p.dvec[grow] : 0.f;
         const float c2 = p.scale_log2;
+        const int col0 = h * 64;   // this warp's score columns
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             ok = mbar_wait(smem_u32(&bars.s_full), j & 1, &abort_flag);
@@ -194,34 +264,46 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             const int key0 = j * TB;
-            int lim = p.Sk - key0;
-            if (p.causal) lim = min(lim, row + p.causal_off - key0 + 1);
+            // a full tile: every key exists and every row of the tile sees all of them
+            const bool full = key0 + TB <= p.Sk && (!p.causal || key0 + TB - 1 <= q0 + p.causal_off);
+            int lim = p.Sk - key0 - col0;
+            if (p.causal) lim = min(lim, row + p.causal_off - key0 + 1 - col0);
             if (!row_ok) lim = 0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t s[32], dp[32];
-                tmem_ld32(tS + lane_off + c * 32, s);
-                tmem_ld32(tP + lane_off + c * 32, dp);
+            // phase A: P for this warp's 64 columns, kept in registers
+            float pv[64];
+            {
+                uint32_t s[64];
+                tmem_ld32(tS + lane_off + col0, *reinterpret_cast<uint32_t(*)[32]>(s));
+                tmem_ld32(tS + lane_off + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
                 tmem_ld_wait();
-                uint32_t pk[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float d0 = 0.f, d1 = 0.f;
-                    const int col = c * 32 + 2 * k;
-                    if (col < lim)
-                        d0 = ex2_approx(__uint_as_float(s[2 * k]) * c2 - lse2) * (__uint_as_float(dp[2 * k]) - dvr);
-                    if (col + 1 < lim)
-                        d1 = ex2_approx(__uint_as_float(s[2 * k + 1]) * c2 - lse2) * (__uint_as_float(dp[2 * k + 1]) - dvr);
-                    pk[k] = pack_bf16x2(d0, d1);
+                for (int k = 0; k < 64; ++k) {
+                    const float e = ex2_approx(fmaf(__uint_as_float(s[k]), c2, -lse2));
+                    pv[k] = (full || k < lim) ? e : 0.f;
                 }
-                // columns 16c .. 16c+15 hold S chunk c/2, already read
-                tmem_st16(tS + lane_off + c * 16, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7], pk[8], pk[9],
-                          pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars.pa));
+            // phase B: dS = P (dP - D_r), as bf16 into this warp's 32 columns of the dS region
+            ok = mbar_wait(smem_u32(&bars.dp_full), j & 1, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t d[32];
+                tmem_ld32(tP + lane_off + col0 + 32 * c, d);
+                tmem_ld_wait();
+                float ds[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ds[k] = pv[32 * c + k] * (__uint_as_float(d[k]) - dvr);
+                pack_store16(tdS + lane_off + h * 32 + 16 * c, ds);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&bars.pb));
         }
         if (!ok) bt_timeout(&abort_flag, p.status);
         // epilogue: dQ = scale * (dS K summed over key tiles); rows with no key get 0
@@ -232,23 +314,11 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if (!have) bt_timeout(&abort_flag, p.status);
             tc_fence_after();
         }
-        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq) + grow * D;
+        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.dq) + (row_ok ? grow : 0) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            if (have) {
-                tmem_ld32(tQ + lane_off + c * 32, o);
-                tmem_ld_wait();
-            }
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                pk[k] = have ? pack_bf16x2(__uint_as_float(o[2 * k]) * p.scale, __uint_as_float(o[2 * k + 1]) * p.scale) : 0u;
-            if (row_ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(dq + c * 32);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-            }
+        for (int c = 0; c < D / 64; ++c) {
+            const int cc = h * (D / 64) + c;   // 32-column chunk of dQ
+            tmem_to_bf16(tQ + lane_off + cc * 32, have, p.scale, row_ok, dq + cc * 32);
         }
     }
     tc_fence_before();
@@ -273,9 +343,11 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sK = sbase + C::A_OFF, sV = sK + C::TILE, sRing = sbase + C::RING_OFF;
-    float *tab = reinterpret_cast<float *>(smem_raw + (sbase - smem_u32(smem_raw)) + C::TAB_OFF);   // [2][2][128]
-    const int key0 = blockIdx.x * TB;
-    const int bk = blockIdx.y, b = bk / p.Hkv, kvh = bk % p.Hkv;
+    float *tab = reinterpret_cast<float *>(smem_raw + (sbase - smem_u32(smem_raw)) + C::TAB_OFF);
+    // the key tiles seen by the most query tiles (the first ones, under a causal mask) go first
+    const int BK = p.B * p.Hkv;
+    const int key0 = (int)(blockIdx.x / BK) * TB;
+    const int bk = blockIdx.x % BK, b = bk / p.Hkv, kvh = bk % p.Hkv;
     const int G = p.Hq / p.Hkv;
     // query tiles that see a key of this block: from the first row that sees key0
     int q_first = p.causal ? max(0, key0 - p.causal_off) : 0;
@@ -284,19 +356,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const int per_head = max(0, n_qt - q_first);
     const int n = G * per_head;   // steps: (head g, query tile) pairs
     if (warp == 0) tmem_alloc(smem_u32(&tmem_sh), TMEM_COLS);
-    if (tid == 32) {
-        mbar_init(smem_u32(&bars.a_full), 1);
-        for (int s = 0; s < C::RING; ++s) {
-            mbar_init(smem_u32(&bars.full[s]), 1);
-            mbar_init(smem_u32(&bars.empty[s]), 1);
-        }
-        mbar_init(smem_u32(&bars.s_full), 1);
-        mbar_init(smem_u32(&bars.p_full), 4);
-        mbar_init(smem_u32(&bars.done), 1);
-        mbar_init(smem_u32(&bars.drain), 1);
-        abort_flag = 0;
-        mbar_init_fence();
-    }
+    if (tid == 32) init_bars<D>(bars, abort_flag);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -331,101 +391,154 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         auto wait_full = [&](int m) {
             return mbar_wait_spin(smem_u32(&bars.full[m % C::RING]), (m / C::RING) & 1, &abort_flag);
         };
-        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag);
-        if (ok) ok = wait_full(0) && wait_full(1);
+        auto ring = [&](int m) { return sRing + (m % C::RING) * C::TILE; };
+        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag) && wait_full(0);
         if (ok) {
             tc_fence_after();
-            issue_ss<D>(tS, sK, sRing + 0 * C::TILE);          // S^T = K Q_0^T
-            issue_ss<D>(tP, sV, sRing + 1 * C::TILE);          // dP^T = V dO_0^T
+            issue_ss<D>(tS, sK, ring(0));          // S^T = K Q_0^T
             mma_commit(smem_u32(&bars.s_full));
+            ok = wait_full(1);
+        }
+        if (ok) {
+            tc_fence_after();
+            issue_ss<D>(tP, sV, ring(1));          // dP^T = V dO_0^T
+            mma_commit(smem_u32(&bars.dp_full));
         }
         for (int j = 0; j < n && ok; ++j) {
             const int mq_ = 2 * j, mg_ = 2 * j + 1;
-            ok = mbar_wait_spin(smem_u32(&bars.p_full), j & 1, &abort_flag);
+            // phase A: P^T is in TMEM
+            ok = mbar_wait_spin(smem_u32(&bars.pa), j & 1, &abort_flag);
             if (!ok) break;
             tc_fence_after();
-            issue_ts<D>(tV, tS, sRing + (mg_ % C::RING) * C::TILE, j > 0);   // dV += P^T dO
-            issue_ts<D>(tK, tP, sRing + (mq_ % C::RING) * C::TILE, j > 0);   // dK += dS^T Q
-            mma_commit(smem_u32(&bars.empty[mq_ % C::RING]));
-            mma_commit(smem_u32(&bars.empty[mg_ % C::RING]));
+            issue_ts<D>(tV, tS, tS + 64, ring(mg_), j > 0);    // dV += P^T dO_j
+            mma_commit(smem_u32(&bars.empty[mg_ % C::RING]));   // dO_j is done
             if (j + 1 < n) {
-                ok = wait_full(mq_ + 2) && wait_full(mg_ + 2);
+                ok = wait_full(mq_ + 2);
                 if (!ok) break;
                 tc_fence_after();
-                issue_ss<D>(tS, sK, sRing + ((mq_ + 2) % C::RING) * C::TILE);
-                issue_ss<D>(tP, sV, sRing + ((mg_ + 2) % C::RING) * C::TILE);
+                issue_ss<D>(tS, sK, ring(mq_ + 2));
                 mma_commit(smem_u32(&bars.s_full));
+            }
+            // phase B: dS^T is in TMEM
+            ok = mbar_wait_spin(smem_u32(&bars.pb), j & 1, &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_ts<D>(tK, tP, tP + 64, ring(mq_), j > 0);    // dK += dS^T Q_j
+            mma_commit(smem_u32(&bars.empty[mq_ % C::RING]));   // Q_j is done
+            if (j + 1 < n) {
+                ok = wait_full(mg_ + 2);
+                if (!ok) break;
+                tc_fence_after();
+                issue_ss<D>(tP, sV, ring(mg_ + 2));
+                mma_commit(smem_u32(&bars.dp_full));
             }
         }
         if (ok) mma_commit(smem_u32(&bars.done));
         else bt_timeout(&abort_flag, p.status);
         mma_commit(smem_u32(&bars.drain));
         mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
+    } else if (warp == 2 && n > 0) {
+        // ------------------------------------------------------------ per-query lse (base 2), D
+        bool ok = true;
+        for (int m = 0; m < n; ++m) {
+            const int st = m % TSTAGES;
+            ok = mbar_wait(smem_u32(&bars.t_empty[st]), ((m / TSTAGES) & 1) ^ 1, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            int hq, qt;
+            step_at(m, hq, qt);
+            float *tl = tab + st * 2 * TB, *td = tl + TB;
+            const long long row0 = ((long long)b * p.Hq + hq) * p.Sq;
+#pragma unroll
+            for (int i = 0; i < TB / 32; ++i) {
+                const int c = lane + 32 * i, q = qt * TB + c;
+                tl[c] = q < p.Sq ? p.lse[row0 + q] * kLog2e : INFINITY;
+                td[c] = q < p.Sq ? p.dvec[row0 + q] : 0.f;
+            }
+            mbar_arrive(smem_u32(&bars.t_full[st]));
+        }
+        if (!ok) bt_timeout(&abort_flag, p.status);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ compute: P^T, dS^T
-        const int r = tid - 128, key = key0 + r;
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int q4 = warp & 3, h = (warp - 4) >> 2;
+        const int r = q4 * 32 + lane, key = key0 + r;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const float c2 = p.scale_log2;
+        const int col0 = h * 64;   // this warp's query columns
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             int hq, qt;
             step_at(j, hq, qt);
-            const int qbase = qt * TB;
-            // this step's per-query lse (base 2) and D, double-buffered between steps
-            float *tl = tab + (j & 1) * 2 * TB, *td = tl + TB;
-            {
-                const int q = qbase + r;
-                const long long gq = ((long long)b * p.Hq + hq) * p.Sq + q;
-                tl[r] = q < p.Sq ? p.lse[gq] * kLog2e : INFINITY;
-                td[r] = q < p.Sq ? p.dvec[gq] : 0.f;
-            }
-            // every warp passes this barrier once per step, even after a failed wait (then it
-            // skips the work), so no warp can wait here for one that has left the loop
-            named_barrier(1, 128);
-            if (!ok) continue;
-            ok = mbar_wait(smem_u32(&bars.s_full), j & 1, &abort_flag);
+            const int qbase = qt * TB, st = j % TSTAGES;
+            ok = mbar_wait(smem_u32(&bars.s_full), j & 1, &abort_flag) &&
+                 mbar_wait(smem_u32(&bars.t_full[st]), (j / TSTAGES) & 1, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) continue;
+            if (!ok) break;
             tc_fence_after();
-            // query column q is visible to this key iff q < Sq, key < Sk and (causal) key <= q + off
-            int qmin = 0;   // first visible column of the tile
-            if (p.causal) qmin = key - p.causal_off - qbase;
-            const int qmax = min(TB, p.Sq - qbase);   // columns past the sequence are out
-            const bool key_ok = key < p.Sk;
+            const float4 *tl4 = reinterpret_cast<const float4 *>(tab + st * 2 * TB + col0);
+            const float4 *td4 = reinterpret_cast<const float4 *>(tab + st * 2 * TB + TB + col0);
+            // query column q is visible to this key iff (causal) key <= q + off; columns past
+            // Sq have lse = +inf (P = 0) and zero Q, dO rows; keys past Sk are never stored
+            const bool full = !p.causal || key0 + TB - 1 - p.causal_off <= qbase;
+            const int qmin = p.causal ? key - p.causal_off - qbase - col0 : INT_MIN;
+            // phase A: P^T for this warp's 64 columns (fp32 in registers, bf16 into TMEM)
+            float pv[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t s[32], dp[32];
-                tmem_ld32(tS + lane_off + c * 32, s);
-                tmem_ld32(tP + lane_off + c * 32, dp);
+            for (int c = 0; c < 2; ++c) {
+                uint32_t s[32];
+                tmem_ld32(tS + lane_off + col0 + 32 * c, s);
                 tmem_ld_wait();
-                uint32_t pp[16], pd[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
-                    const int col = c * 32 + 2 * k;
-                    if (key_ok && col >= qmin && col < qmax) {
-                        p0 = ex2_approx(__uint_as_float(s[2 * k]) * c2 - tl[col]);
-                        d0 = p0 * (__uint_as_float(dp[2 * k]) - td[col]);
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 l = tl4[8 * c + k4];
+                    const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * k4 + e;
+                        const float x = ex2_approx(fmaf(__uint_as_float(s[k]), c2, -lv[e]));
+                        pv[32 * c + k] = (full || 32 * c + k >= qmin) ? x : 0.f;
                     }
-                    if (key_ok && col + 1 >= qmin && col + 1 < qmax) {
-                        p1 = ex2_approx(__uint_as_float(s[2 * k + 1]) * c2 - tl[col + 1]);
-                        d1 = p1 * (__uint_as_float(dp[2 * k + 1]) - td[col + 1]);
-                    }
-                    pp[k] = pack_bf16x2(p0, p1);
-                    pd[k] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(tS + lane_off + c * 16, pp[0], pp[1], pp[2], pp[3], pp[4], pp[5], pp[6], pp[7], pp[8], pp[9],
-                          pp[10], pp[11], pp[12], pp[13], pp[14], pp[15]);
-                tmem_st16(tP + lane_off + c * 16, pd[0], pd[1], pd[2], pd[3], pd[4], pd[5], pd[6], pd[7], pd[8], pd[9],
-                          pd[10], pd[11], pd[12], pd[13], pd[14], pd[15]);
+                pack_store16(tS + lane_off + col0 + 16 * c, *reinterpret_cast<const float(*)[32]>(pv + 32 * c));
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&bars.pa));
+            // phase B: dS^T = P^T (dP^T - D_q), bf16 into TMEM
+            ok = mbar_wait(smem_u32(&bars.dp_full), j & 1, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t d[32];
+                tmem_ld32(tP + lane_off + col0 + 32 * c, d);
+                tmem_ld_wait();
+                float ds[32];
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 dd = td4[8 * c + k4];
+                    const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * k4 + e;
+                        ds[k] = pv[32 * c + k] * (__uint_as_float(d[k]) - dv[e]);
+                    }
+                }
+                pack_store16(tP + lane_off + col0 + 16 * c, ds);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&bars.pb));
+                mbar_arrive(smem_u32(&bars.t_empty[st]));
+            }
         }
         if (!ok) bt_timeout(&abort_flag, p.status);
-        // epilogue: dK = scale * dS^T Q, dV = P^T dO (zero when no query sees this key)
+        // epilogue: dK = scale * dS^T Q (warps of half 0), dV = P^T dO (half 1); zero when no
+        // query sees this key
         bool have = false;
         if (ok && n > 0) {
             have = mbar_wait(smem_u32(&bars.done), 0, &abort_flag);
@@ -433,36 +546,13 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (!have) bt_timeout(&abort_flag, p.status);
             tc_fence_after();
         }
-        // the TMEM loads are warp-collective (.sync.aligned): every lane issues them, and only
-        // the stores of keys past Sk are skipped
         const bool key_ok = key < p.Sk;
         const long long gk = (long long)bk * p.Sk + (key_ok ? key : 0);
-        __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.dk) + gk * D;
-        __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.dv) + gk * D;
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(h ? p.dv : p.dk) + gk * D;
+        const uint32_t src = (h ? tV : tK) + lane_off;
+        const float sc = h ? 1.f : p.scale;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t src = (h ? tV : tK) + lane_off;
-            const float sc = h ? 1.f : p.scale;
-            __nv_bfloat16 *out = h ? dv : dk;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                if (have) {
-                    tmem_ld32(src + c * 32, o);
-                    tmem_ld_wait();
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    pk[k] = have ? pack_bf16x2(__uint_as_float(o[2 * k]) * sc, __uint_as_float(o[2 * k + 1]) * sc) : 0u;
-                if (key_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                }
-            }
-        }
+        for (int c = 0; c < D / 32; ++c) tmem_to_bf16(src + c * 32, have, sc, key_ok, out + c * 32);
     }
     tc_fence_before();
     __syncwarp();
@@ -493,8 +583,10 @@ cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
         !make_bf16_tile_map_strided(&mk, p.k, D, p.Sk, p.Hkv, p.B, D, ks, ks * p.Hkv, TB) ||
         !make_bf16_tile_map_strided(&mv, p.v, D, p.Sk, p.Hkv, p.B, D, ks, ks * p.Hkv, TB))
         return cudaErrorInvalidValue;
-    bwd_dkdv_tc_kernel<D><<<dim3((p.Sk + TB - 1) / TB, p.B * p.Hkv), NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
-    bwd_dq_tc_kernel<D><<<dim3((p.Sq + TB - 1) / TB, p.B * p.Hq), NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
+    const unsigned nkv = (unsigned)((p.Sk + TB - 1) / TB) * (unsigned)(p.B * p.Hkv);
+    const unsigned nq = (unsigned)((p.Sq + TB - 1) / TB) * (unsigned)(p.B * p.Hq);
+    bwd_dkdv_tc_kernel<D><<<nkv, NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
+    bwd_dq_tc_kernel<D><<<nq, NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
     count_launches(2);
     return cudaGetLastError();
 }
@@ -508,7 +600,10 @@ bool attn_bwd_tc_supported(const BwdProblem &p) {
                         reinterpret_cast<uintptr_t>(p.dq) | reinterpret_cast<uintptr_t>(p.dk) |
                         reinterpret_cast<uintptr_t>(p.dv);
     if ((a & 15u) != 0) return false;
-    if ((p.Sk + TB - 1) / TB >= 65536 * 32 || (long long)p.B * p.Hq >= 65536) return false;
+    // one-dimensional grids of (row tile, batch x head) CTAs
+    const long long nkv = (long long)((p.Sk + TB - 1) / TB) * p.B * p.Hkv;
+    const long long nq = (long long)((p.Sq + TB - 1) / TB) * p.B * p.Hq;
+    if (nkv >= (1LL << 31) || nq >= (1LL << 31)) return false;
     return tensor_map_encoder() != nullptr;
 }
 
