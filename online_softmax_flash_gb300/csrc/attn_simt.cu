@@ -210,54 +210,68 @@ attn_simt_kernel(const AttnProblem p) {
 }
 
 // Log-sum-exp combine of split partial states: M = max_s m_s, w_s = 2^(m_s - M),
-// O = sum_s w_s acc_s / sum_s w_s l_s, lse = (M + log2 L) ln 2.  One warp per output row: the
-// lanes first take one split's (m, l) each (M and L by warp reductions), then each lane sums its
-// columns over the splits with the weights broadcast by shuffles; the split loop is unrolled so
-// its loads are in flight together.
-template <typename T>
+// O = sum_s w_s acc_s / sum_s w_s l_s, lse = (M + log2 L) ln 2.  One thread per four columns of
+// an output row.  The splits are taken eight at a time with every load of a group issued
+// together, and the group folds into running (M, L, O) by the same rescaling rule, so a
+// combine over up to eight splits waits for memory once.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) {
+    constexpr int SG = 8;   // splits per load group
     const long long rows_total = (long long)p.B * p.Hq * p.Sq;
-    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int groups = (p.D + 3) >> 2;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = idx / groups;
+    const int c0 = (int)(idx - row * groups) * 4;
     if (row >= rows_total) return;
-    float M = -INFINITY;
-    for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, p.part_m[(size_t)s * rows_total + row]);
-    M = warp_max(M);
-    const float Mref = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = lane; s < p.splits; s += 32)
-        L += p.part_l[(size_t)s * rows_total + row] * ex2_approx(p.part_m[(size_t)s * rows_total + row] - Mref);
-    L = warp_sum(L);
+    float M = -INFINITY, L = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < p.splits; s0 += SG) {
+        float ms[SG], ls[SG], acc[SG][4];
+#pragma unroll
+        for (int i = 0; i < SG; ++i) {
+            const int sp = s0 + i;
+            ms[i] = -INFINITY;
+            ls[i] = 0.f;
+            acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            if (sp < p.splits) {
+                const size_t r = (size_t)sp * rows_total + row;
+                ms[i] = p.part_m[r];
+                ls[i] = p.part_l[r];
+                const float *A = p.part_acc + r * p.D + c0;
+                if (VEC) {
+                    const float4 v = *reinterpret_cast<const float4 *>(A);
+                    acc[i][0] = v.x; acc[i][1] = v.y; acc[i][2] = v.z; acc[i][3] = v.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (c0 + e < p.D) acc[i][e] = A[e];
+                }
+            }
+        }
+        float mg = M;
+#pragma unroll
+        for (int i = 0; i < SG; ++i) mg = fmaxf(mg, ms[i]);
+        const float mref = mg == -INFINITY ? 0.f : mg;
+        const float sc = ex2_approx(M - mref);   // 0 while nothing has been seen
+        L *= sc;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] *= sc;
+#pragma unroll
+        for (int i = 0; i < SG; ++i) {
+            const float w = ex2_approx(ms[i] - mref);
+            L += w * ls[i];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] += w * acc[i][e];
+        }
+        M = mg;
+    }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int b = (int)(row / ((long long)p.Hq * p.Sq));
     const int hq = (int)((row / p.Sq) % p.Hq);
     T *Og = static_cast<T *>(p.o) + o_at(p, b, hq, row % p.Sq);
-    constexpr int CMAX = 8;   // columns per lane (D <= 256)
-    float a[CMAX];
 #pragma unroll
-    for (int k = 0; k < CMAX; ++k) a[k] = 0.f;
-    for (int s0 = 0; s0 < p.splits; s0 += 32) {
-        // this lane's weight for split s0 + lane
-        const int sl = s0 + lane;
-        const float wl = sl < p.splits ? ex2_approx(p.part_m[(size_t)sl * rows_total + row] - Mref) : 0.f;
-        const int n = min(32, p.splits - s0);
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-            const float w = __shfl_sync(0xffffffffu, wl, j);
-            const float *acc = p.part_acc + ((size_t)(s0 + j) * rows_total + row) * p.D;
-#pragma unroll
-            for (int k = 0; k < CMAX; ++k) {
-                const int c = lane + 32 * k;
-                if (c < p.D) a[k] += w * acc[c];
-            }
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < CMAX; ++k) {
-        const int c = lane + 32 * k;
-        if (c < p.D) Og[c] = from_f32<T>(a[k] * inv);
-    }
-    if (p.lse && lane == 0) p.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    for (int e = 0; e < 4; ++e)
+        if (c0 + e < p.D) Og[c0 + e] = from_f32<T>(a[e] * inv);
+    if (p.lse && c0 == 0) p.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
 template <typename T, int DP, int BM>
@@ -312,11 +326,16 @@ cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t s) {
 
 cudaError_t launch_attn_combine(const AttnProblem &p, cudaStream_t s) {
     const long long rows_total = (long long)p.B * p.Hq * p.Sq;
-    const unsigned blocks = (unsigned)((rows_total + 7) / 8);
-    if (p.dtype == OSF_F32)
-        attn_combine_kernel<float><<<blocks, 256, 0, s>>>(p);
-    else
-        attn_combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+    const long long threads = rows_total * ((p.D + 3) / 4);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    const bool vec = p.D % 4 == 0;   // part_acc rows are then 16-byte aligned
+    if (p.dtype == OSF_F32) {
+        if (vec) attn_combine_kernel<float, true><<<blocks, 256, 0, s>>>(p);
+        else attn_combine_kernel<float, false><<<blocks, 256, 0, s>>>(p);
+    } else {
+        if (vec) attn_combine_kernel<__nv_bfloat16, true><<<blocks, 256, 0, s>>>(p);
+        else attn_combine_kernel<__nv_bfloat16, false><<<blocks, 256, 0, s>>>(p);
+    }
     count_launches(1);
     return cudaGetLastError();
 }
