@@ -96,7 +96,9 @@ TRAFFIC = {
                      "bytes": 1020.95e6, "scope": "softmax_rows_onchip_kernel<8>, one launch"},
     "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "1369193089605318",
                    "bytes": 760.90e6, "scope": "step: chunk state + chunk normalise kernels"},
-    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_simt.cu", "sha": "ea58427b628cd84b",
+    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "5dc2a8c67e0fdd8a",
+                            "bytes": 320.96e6, "scope": "bwd_dkdv_tc_kernel<128>, one launch"},
+    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_simt.cu", "sha": "7e9f09b65c386443",
                              "bytes": 3.17e6, "scope": "attn_simt_kernel<float,64,64>, one launch"},
 }
 
