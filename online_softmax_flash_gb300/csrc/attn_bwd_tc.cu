@@ -3,8 +3,10 @@
 // from the forward's log-sum-exp), with every product a tcgen05.mma into TMEM and the operand
 // tiles streamed by TMA, as in the forward kernel.
 //
-// Warp roles (384 threads): warp 0 issues the TMA loads, warp 1 the MMAs, warp 2 (dK/dV kernel)
-// fills a small ring of per-query lse / D tables, warps 4-11 compute.  Compute warp w owns the
+// Warp roles (384 threads): warp 0 issues the TMA loads, warps 1 and 3 the MMAs (one thread each,
+// two independent instruction streams: one thread cannot issue tcgen05.mma as fast as the tensor
+// pipe runs M128 N128 products), warp 2 (dK/dV kernel) fills a small ring of per-query lse / D
+// tables, warps 4-11 compute.  Compute warp w owns the
 // TMEM lanes 32 (w % 4) .. +31 (one row of the tile per thread) and one half of the 128 columns,
 // h = (w - 4) / 4, so two warps share each sub-partition.
 //
@@ -16,10 +18,11 @@
 // of every query head of the group that sees these keys.  Per step j (query tile Q_j, dO_j):
 //   S^T = K Q_j^T, dP^T = V dO_j^T;  A: P^T as bf16 over the first half of each warp's S^T
 //   columns, then dV += P^T dO_j;  B: dS^T over dP^T, then dK += dS^T Q_j.
-//   Pipe order: dV_j, S^T_{j+1} (while phase B runs), dK_j, dP^T_{j+1} (while phase A of j+1 runs).
+//   Issuer A: dV_j then S^T_{j+1} (while phase B runs); issuer B: dK_j then dP^T_{j+1} (while
+//   phase A of step j+1 runs).
 // dQ kernel: one CTA per (b, q head, 128 query rows), Q and dO resident, K_j, V_j streamed:
-//   S = Q K_j^T, dP = dO V_j^T;  A releases S (S_{j+1} is issued at once);  B writes dS as bf16
-//   into its own columns, then dQ += dS K_j and dP_{j+1}.
+//   S = Q K_j^T, dP = dO V_j^T;  phase A releases S (issuer A issues S_{j+1} at once);  phase B
+//   writes dS as bf16 into its own columns, then issuer B issues dQ += dS K_j and dP_{j+1}.
 //
 // TMEM (512 columns).  dK/dV: S^T [0,128), dP^T [128,256), dK [256,256+D), dV [256+D,256+2D).
 // dQ: S [0,128), dP [128,256), dQ [256,256+D), dS (bf16) [256+D,256+D+64).
@@ -64,7 +67,7 @@ struct BtBars {
     uint64_t a_full;
     uint64_t full[MAX_RING], empty[MAX_RING];
     uint64_t t_full[TSTAGES], t_empty[TSTAGES];
-    uint64_t s_full, dp_full, pa, pb, done, drain;
+    uint64_t s_full, dp_full, pa, pb, done, drain[2];
 };
 
 __device__ __forceinline__ void bt_timeout(volatile int *abort, int *status) {
@@ -131,7 +134,7 @@ __device__ __forceinline__ void init_bars(BtBars &bars, volatile int &abort_flag
     mbar_init(smem_u32(&bars.a_full), 1);
     for (int s = 0; s < C::RING; ++s) {
         mbar_init(smem_u32(&bars.full[s]), 1);
-        mbar_init(smem_u32(&bars.empty[s]), 1);
+        mbar_init(smem_u32(&bars.empty[s]), 2);   // one release from each issuer
     }
     for (int s = 0; s < TSTAGES; ++s) {
         mbar_init(smem_u32(&bars.t_full[s]), 32);
@@ -141,8 +144,9 @@ __device__ __forceinline__ void init_bars(BtBars &bars, volatile int &abort_flag
     mbar_init(smem_u32(&bars.dp_full), 1);
     mbar_init(smem_u32(&bars.pa), NCW);
     mbar_init(smem_u32(&bars.pb), NCW);
-    mbar_init(smem_u32(&bars.done), 1);
-    mbar_init(smem_u32(&bars.drain), 1);
+    mbar_init(smem_u32(&bars.done), 2);
+    mbar_init(smem_u32(&bars.drain[0]), 1);
+    mbar_init(smem_u32(&bars.drain[1]), 1);
     abort_flag = 0;
     mbar_init_fence();
 }
@@ -196,56 +200,67 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             bt_timeout(&abort_flag, p.status);
             bt_settle();
         }
-    } else if (warp == 1 && lane == 0 && n > 0) {
-        // ------------------------------------------------------------ MMA issue
+    } else if ((warp == 1 || warp == 3) && lane == 0 && n > 0) {
+        // ------------------------------------------------------------ MMA issue, two threads
+        // Issuer A (warp 1): S = Q K_j^T.  Issuer B (warp 3): dP = dO V_j^T and dQ += dS K_j.
+        // Neither touches the other's TMEM columns; a ring slot is free once both have released
+        // it (B releases the V slots twice).  B's commit after dP_{j+1} covers dQ_j, so phase B
+        // of step j+1 may overwrite dS.
+        const bool is_a = warp == 1;
         auto wait_full = [&](int m) {
             return mbar_wait_spin(smem_u32(&bars.full[m % C::RING]), (m / C::RING) & 1, &abort_flag);
         };
         auto ring = [&](int m) { return sRing + (m % C::RING) * C::TILE; };
-        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag) && wait_full(0);
+        auto release = [&](int m) { mma_commit(smem_u32(&bars.empty[m % C::RING])); };
+        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag) && wait_full(is_a ? 0 : 1);
         if (ok) {
             tc_fence_after();
-            issue_ss<D>(tS, sQ, ring(0));                      // S = Q K_0^T
-            mma_commit(smem_u32(&bars.s_full));
-            ok = wait_full(1);
-        }
-        if (ok) {
-            tc_fence_after();
-            issue_ss<D>(tP, sG, ring(1));                      // dP = dO V_0^T
-            mma_commit(smem_u32(&bars.dp_full));
-            mma_commit(smem_u32(&bars.empty[1 % C::RING]));     // V_0 is done
+            if (is_a) {
+                issue_ss<D>(tS, sQ, ring(0));                  // S = Q K_0^T
+                mma_commit(smem_u32(&bars.s_full));
+                release(0);
+            } else {
+                issue_ss<D>(tP, sG, ring(1));                  // dP = dO V_0^T
+                mma_commit(smem_u32(&bars.dp_full));
+                release(1);
+                release(1);
+            }
         }
         for (int j = 0; j < n && ok; ++j) {
             const int mk_ = 2 * j;
-            // phase A of step j has read S: the next S may overwrite it
-            ok = mbar_wait_spin(smem_u32(&bars.pa), j & 1, &abort_flag);
-            if (!ok) break;
-            if (j + 1 < n) {
+            if (is_a) {
+                // phase A of step j has read S: the next S may overwrite it
+                ok = mbar_wait_spin(smem_u32(&bars.pa), j & 1, &abort_flag);
+                if (!ok || j + 1 >= n) continue;
                 ok = wait_full(mk_ + 2);
                 if (!ok) break;
                 tc_fence_after();
                 issue_ss<D>(tS, sQ, ring(mk_ + 2));
                 mma_commit(smem_u32(&bars.s_full));
-            }
-            // phase B has read dP and written dS
-            ok = mbar_wait_spin(smem_u32(&bars.pb), j & 1, &abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_ts<D>(tQ, tdS, tdS + 32, ring(mk_), j > 0);   // dQ += dS K_j
-            mma_commit(smem_u32(&bars.empty[mk_ % C::RING]));   // K_j is done
-            if (j + 1 < n) {
-                ok = wait_full(mk_ + 3);
+                release(mk_ + 2);
+            } else {
+                // phase B has read dP and written dS
+                ok = mbar_wait_spin(smem_u32(&bars.pb), j & 1, &abort_flag) && wait_full(mk_);
                 if (!ok) break;
                 tc_fence_after();
-                issue_ss<D>(tP, sG, ring(mk_ + 3));
-                mma_commit(smem_u32(&bars.dp_full));
-                mma_commit(smem_u32(&bars.empty[(mk_ + 3) % C::RING]));
+                issue_ts<D>(tQ, tdS, tdS + 32, ring(mk_), j > 0);   // dQ += dS K_j
+                release(mk_);
+                if (j + 1 < n) {
+                    ok = wait_full(mk_ + 3);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_ss<D>(tP, sG, ring(mk_ + 3));
+                    mma_commit(smem_u32(&bars.dp_full));
+                    release(mk_ + 3);
+                    release(mk_ + 3);
+                }
             }
         }
         if (ok) mma_commit(smem_u32(&bars.done));
         else bt_timeout(&abort_flag, p.status);
-        mma_commit(smem_u32(&bars.drain));
-        mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
+        const uint32_t dr = smem_u32(&bars.drain[is_a ? 0 : 1]);
+        mma_commit(dr);
+        mbar_wait(dr, 0, nullptr, 20000000ull);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ compute: dS, then dQ out
         const int q4 = warp & 3, h = (warp - 4) >> 2;
@@ -386,57 +401,50 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             bt_timeout(&abort_flag, p.status);
             bt_settle();
         }
-    } else if (warp == 1 && lane == 0 && n > 0) {
-        // ------------------------------------------------------------ MMA issue
+    } else if ((warp == 1 || warp == 3) && lane == 0 && n > 0) {
+        // ------------------------------------------------------------ MMA issue, two threads
+        // Issuer A (warp 1): S^T = K Q_j^T and dV += P^T dO_j.  Issuer B (warp 3):
+        // dP^T = V dO_j^T and dK += dS^T Q_j.  A only touches S^T and dV, B only dP^T and dK;
+        // Q_j and dO_j each feed one product of each side, so each side releases every slot once.
+        const bool is_a = warp == 1;
         auto wait_full = [&](int m) {
             return mbar_wait_spin(smem_u32(&bars.full[m % C::RING]), (m / C::RING) & 1, &abort_flag);
         };
         auto ring = [&](int m) { return sRing + (m % C::RING) * C::TILE; };
-        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag) && wait_full(0);
+        auto release = [&](int m) { mma_commit(smem_u32(&bars.empty[m % C::RING])); };
+        const int own = is_a ? 0 : 1;              // stream offset of this side's score operand
+        const uint32_t tX = is_a ? tS : tP, sX = is_a ? sK : sV;
+        bool ok = mbar_wait_spin(smem_u32(&bars.a_full), 0, &abort_flag) && wait_full(own);
         if (ok) {
             tc_fence_after();
-            issue_ss<D>(tS, sK, ring(0));          // S^T = K Q_0^T
-            mma_commit(smem_u32(&bars.s_full));
-            ok = wait_full(1);
-        }
-        if (ok) {
-            tc_fence_after();
-            issue_ss<D>(tP, sV, ring(1));          // dP^T = V dO_0^T
-            mma_commit(smem_u32(&bars.dp_full));
+            issue_ss<D>(tX, sX, ring(own));        // S^T = K Q_0^T  /  dP^T = V dO_0^T
+            mma_commit(smem_u32(is_a ? &bars.s_full : &bars.dp_full));
+            release(own);
         }
         for (int j = 0; j < n && ok; ++j) {
-            const int mq_ = 2 * j, mg_ = 2 * j + 1;
-            // phase A: P^T is in TMEM
-            ok = mbar_wait_spin(smem_u32(&bars.pa), j & 1, &abort_flag);
+            // A: P^T is in TMEM, dV += P^T dO_j.  B: dS^T is in TMEM, dK += dS^T Q_j.
+            const int other = 2 * j + 1 - own;     // dO_j for A, Q_j for B
+            ok = mbar_wait_spin(smem_u32(is_a ? &bars.pa : &bars.pb), j & 1, &abort_flag) && wait_full(other);
             if (!ok) break;
             tc_fence_after();
-            issue_ts<D>(tV, tS, tS + 64, ring(mg_), j > 0);    // dV += P^T dO_j
-            mma_commit(smem_u32(&bars.empty[mg_ % C::RING]));   // dO_j is done
+            if (is_a) issue_ts<D>(tV, tS, tS + 64, ring(other), j > 0);
+            else issue_ts<D>(tK, tP, tP + 64, ring(other), j > 0);
+            release(other);
             if (j + 1 < n) {
-                ok = wait_full(mq_ + 2);
+                const int next = 2 * j + 2 + own;  // Q_{j+1} for A, dO_{j+1} for B
+                ok = wait_full(next);
                 if (!ok) break;
                 tc_fence_after();
-                issue_ss<D>(tS, sK, ring(mq_ + 2));
-                mma_commit(smem_u32(&bars.s_full));
-            }
-            // phase B: dS^T is in TMEM
-            ok = mbar_wait_spin(smem_u32(&bars.pb), j & 1, &abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_ts<D>(tK, tP, tP + 64, ring(mq_), j > 0);    // dK += dS^T Q_j
-            mma_commit(smem_u32(&bars.empty[mq_ % C::RING]));   // Q_j is done
-            if (j + 1 < n) {
-                ok = wait_full(mg_ + 2);
-                if (!ok) break;
-                tc_fence_after();
-                issue_ss<D>(tP, sV, ring(mg_ + 2));
-                mma_commit(smem_u32(&bars.dp_full));
+                issue_ss<D>(tX, sX, ring(next));
+                mma_commit(smem_u32(is_a ? &bars.s_full : &bars.dp_full));
+                release(next);
             }
         }
         if (ok) mma_commit(smem_u32(&bars.done));
         else bt_timeout(&abort_flag, p.status);
-        mma_commit(smem_u32(&bars.drain));
-        mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
+        const uint32_t dr = smem_u32(&bars.drain[own]);
+        mma_commit(dr);
+        mbar_wait(dr, 0, nullptr, 20000000ull);
     } else if (warp == 2 && n > 0) {
         // ------------------------------------------------------------ per-query lse (base 2), D
         bool ok = true;
