@@ -198,7 +198,8 @@ Path choose_path(const AttnProblem &p, const void *Q, const void *K, const void 
     // one or a few query rows per head (G * Sq <= 16): the HBM-bound decode kernel, which reads
     // each K/V byte once for all the query heads of its kv head
     if (p.dtype == OSF_BF16 && decode_supported(p, Q, K, V, O)) return Path::Decode;
-    if (p.dtype == OSF_BF16 && p.Sq > 1 && attn_tc_supported(p, Q, K, V, O)) return Path::TensorCore;
+    // bf16, and fp32 with D = 64 (as bf16 high / low parts)
+    if (p.Sq > 1 && attn_tc_supported(p, Q, K, V, O)) return Path::TensorCore;
     return Path::Simt;
 }
 
@@ -213,8 +214,10 @@ int plan_splits(const AttnProblem &p, Path path, int sm_count, int requested) {
 }
 
 size_t path_workspace(const AttnProblem &p, Path path, int splits) {
-    (void)path;  // every path keeps split partial states in the same layout
-    return partial_bytes(splits, (long long)p.B * p.Hq * p.Sq, p.D);
+    // every path keeps split partial states in the same layout; the tensor-core path keeps the
+    // fp32 operands' bf16 parts after them
+    const size_t part = partial_bytes(splits, (long long)p.B * p.Hq * p.Sq, p.D);
+    return path == Path::TensorCore ? part + align256(attn_tc_extra_bytes(p)) : part;
 }
 
 int run_gqa(AttnProblem &p, Path path, void *workspace, size_t workspace_bytes, int splits,
@@ -227,6 +230,9 @@ int run_gqa(AttnProblem &p, Path path, void *workspace, size_t workspace_bytes, 
     switch (path) {
         case Path::TensorCore:
             if (splits > 1) carve_partials(p, workspace, rows);
+            p.x3_ws = attn_tc_extra_bytes(p) > 0
+                          ? static_cast<void *>(static_cast<char *>(workspace) + partial_bytes(splits, rows, p.D))
+                          : nullptr;
             return launch_status(launch_attn_tc(p, dev->sm_count, s));
         case Path::Decode:
             if (splits > 1) carve_partials(p, workspace, rows);
@@ -298,8 +304,8 @@ int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, 
     if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
     // the larger of the possible paths' needs (alignment decides the path at call time)
     size_t need = partial_bytes(attn_simt_pick_splits(p, dev->sm_count), (long long)B * Hq * Sq, D);
-    if (dtype == OSF_BF16 && Sq > 1 && (D == 64 || D == 128)) {
-        const size_t tc = partial_bytes(attn_tc_pick_splits(p, dev->sm_count), (long long)B * Hq * Sq, D);
+    if (Sq > 1 && ((dtype == OSF_BF16 && (D == 64 || D == 128)) || (dtype == OSF_F32 && D == 64))) {
+        const size_t tc = path_workspace(p, Path::TensorCore, attn_tc_pick_splits(p, dev->sm_count));
         if (tc > need) need = tc;
     }
     if (dtype == OSF_BF16 && (long long)(Hq / Hkv) * Sq <= 16) {

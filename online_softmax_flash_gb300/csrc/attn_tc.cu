@@ -54,20 +54,35 @@ constexpr float kRescaleThreshold = 8.0f;   // base-2 units
 constexpr uint32_t kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KiB)
 constexpr int kMaxStages = 12;
 
-template <int D>
+// X3 (float32 Q, K, V, D = 64): every operand is a sum of bf16 parts and every product a sum
+// of bf16 products with fp32 accumulation.  Q and K have three parts, x = h + m + l with
+// h = bf16(x), m = bf16(x - h), l = bf16(x - h - m) (x to about 2^-26 relative), and
+//   S = Qh Kh^T + Qh Km^T + Qm Kh^T + Qh Kl^T + Ql Kh^T + Qm Km^T
+// drops only terms of about 2^-24 relative: the exponent turns an absolute error of S into a
+// relative error of P, so S must be as good as float32.  V and P (in [0, 1]) have two parts,
+// h and l = bf16(x - h) (about 2^-17 relative), and O += Ph [Vh | Vl] + Pl Vh, with
+// O = O[:, :D] + O[:, D:] at the end.
+template <int D, bool X3>
 struct TcCfg {
     static constexpr uint32_t TILE = BN * D * 2;                 // one [128 x D] bf16 tile (Q, K or V)
     static constexpr uint32_t DBLK = BN * 128;                   // bytes between 64-column blocks
-    // K and V tiles share one ring, filled in the order they are consumed (K0 V0 K1 V1 ...);
-    // the ring takes what the two Q tiles leave of shared memory (5 stages at D = 128).
-    static constexpr int STAGES = (int)((kSmemLimit - 2048 - 2 * TILE) / TILE) < kMaxStages
-                                      ? (int)((kSmemLimit - 2048 - 2 * TILE) / TILE) : kMaxStages;
+    static constexpr int QP = X3 ? 3 : 1, KP = X3 ? 3 : 1, VP = X3 ? 2 : 1;   // parts per operand
+    static constexpr int QT = 2 * QP;                            // resident Q tiles: part p of tile t at 2p + t
+    static constexpr int NPOS = KP + VP;                         // ring positions per key tile
+    // K and V tiles share one ring, filled in the order they are consumed (K0 V0 K1 V1 ..., in
+    // x3 mode K0h K0m K0l V0h V0l ...); the ring takes what the Q tiles leave of shared memory
+    // (5 stages at D = 128, 8 in x3 mode).
+    static constexpr int FIT = (int)((kSmemLimit - 2048 - QT * TILE) / TILE);
+    static constexpr int STAGES = FIT < kMaxStages ? FIT : kMaxStages;
+    static_assert(!X3 || (D == 64 && STAGES >= 2 * NPOS - 2 && TILE == DBLK), "x3 mode is built for D = 64");
     static constexpr uint32_t Q_OFF = 0;
-    static constexpr uint32_t RING_OFF = 2 * TILE;
+    static constexpr uint32_t RING_OFF = QT * TILE;
     static constexpr uint32_t SMEM_BYTES = RING_OFF + STAGES * TILE + 1024;  // + alignment slack
-    static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
+    static constexpr int DO = X3 ? 2 * D : D;                    // TMEM columns of one O accumulator
+    static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + DO;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);
+    static constexpr uint32_t IDESC_PV2 = idesc_bf16_f32(BM, 2 * D, 0, 1);
 };
 
 struct Barriers {
@@ -132,11 +147,14 @@ __device__ __forceinline__ bool item_at(const AttnProblem &p, int n_qb, int n_it
 // Persistent: each CTA walks its work items (item_at) with one pipeline whose state -- ring
 // position, barrier phases -- carries from item to item, so an item's Q tiles and first K/V
 // tiles load while the previous item finishes.
-template <int D>
+template <int D, bool X3>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mv, const AttnProblem p, int n_qb, int n_items) {
-    using C = TcCfg<D>;
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mqm,
+               const __grid_constant__ CUtensorMap mkm, const __grid_constant__ CUtensorMap mql,
+               const __grid_constant__ CUtensorMap mkl, const __grid_constant__ CUtensorMap mvl,
+               const AttnProblem p, int n_qb, int n_items) {
+    using C = TcCfg<D, X3>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_sh;
@@ -183,9 +201,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         // instruction per tile, so neither stream waits behind the other's instruction issue.
         // An item's Q tiles load once the previous item's last Q K^T products have completed.
         const int odd = warp == 2;
-        const CUtensorMap *map = odd ? &mv : &mk;
+        const CUtensorMap *map = odd ? &mv : &mk, *map_lo = odd ? &mvl : &mkl;
         tma_prefetch_desc(map);
-        if (!odd) tma_prefetch_desc(&mq);
+        if (X3) {
+            tma_prefetch_desc(map_lo);
+            if (!odd) tma_prefetch_desc(&mkm);
+        }
+        if (!odd) {
+            tma_prefetch_desc(&mq);
+            if (X3) {
+                tma_prefetch_desc(&mqm);
+                tma_prefetch_desc(&mql);
+            }
+        }
         bool ok = true;
         int gt = 0, qc = 0;   // key tiles streamed so far, Q loads so far
         Item w;
@@ -195,18 +223,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 ok = mbar_wait(smem_u32(&bars.q_empty), (qc & 1) ^ 1, &abort_flag);
                 if (!ok) break;
                 ++qc;
-                mbar_expect_tx(smem_u32(&bars.q_full), w.ntiles * C::TILE);
-                for (int t = 0; t < w.ntiles; ++t)
-                    tma_load_5d(sQ + t * C::TILE, &mq, smem_u32(&bars.q_full), 0, w.q0 + t * BM, 0, w.hq, w.b);
+                mbar_expect_tx(smem_u32(&bars.q_full), w.ntiles * C::TILE * C::QP);
+#pragma unroll
+                for (int part = 0; part < C::QP; ++part)
+                    for (int t = 0; t < w.ntiles; ++t)
+                        tma_load_5d(sQ + (2 * part + t) * C::TILE, part == 0 ? &mq : part == 1 ? &mqm : &mql,
+                                    smem_u32(&bars.q_full), 0, w.q0 + t * BM, 0, w.hq, w.b);
             }
-            for (int j = 0; j < w.n_kv; ++j) {
-                const int n = 2 * (gt + j) + odd;
-                const int st = stage_of(n);
-                ok = mbar_wait(smem_u32(&bars.empty[st]), parity_of(n) ^ 1, &abort_flag);
-                if (!ok) break;
-                mbar_expect_tx(smem_u32(&bars.full[st]), C::TILE);
-                tma_load_5d(sRing + st * C::TILE, map, smem_u32(&bars.full[st]), 0, (w.kt_begin + j) * BN, 0, w.kvh,
-                            w.b);
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+#pragma unroll
+                for (int part = 0; part < (odd ? C::VP : C::KP); ++part) {
+                    const int n = C::NPOS * (gt + j) + (odd ? C::KP : 0) + part;
+                    const int st = stage_of(n);
+                    ok = mbar_wait(smem_u32(&bars.empty[st]), parity_of(n) ^ 1, &abort_flag);
+                    if (!ok) break;
+                    mbar_expect_tx(smem_u32(&bars.full[st]), C::TILE);
+                    const CUtensorMap *mp = part == 0 ? map : (part == 2 || odd) ? map_lo : &mkm;
+                    tma_load_5d(sRing + st * C::TILE, mp, smem_u32(&bars.full[st]), 0, (w.kt_begin + j) * BN, 0,
+                                w.kvh, w.b);
+                }
             }
             gt += w.n_kv;
         }
@@ -225,36 +260,77 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         // Descriptors are built once per operand tile; stepping along K adds the byte offset
         // (>> 4) to the start-address field, which cannot carry out of its 14 bits because
         // shared-memory addresses stay below 256 KiB.
-        auto issue_s = [&](int t, int st) {
-            const uint64_t qd = sdesc_sw128(sQ + t * C::TILE, 16, 1024);
-            const uint64_t kd = sdesc_sw128(sRing + st * C::TILE, 16, 1024);
-            const uint32_t dst = tmem + (t ? C::S_COL1 : C::S_COL0);
+        // Stream positions of key tile g: K parts from NPOS*g, V parts from NPOS*g + KP.  An
+        // operand's parts are waited for and released together.
+        auto wait_parts = [&](int n, int parts) {
+            bool r = true;
+            for (int q = 0; q < parts && r; ++q)
+                r = mbar_wait_spin(smem_u32(&bars.full[stage_of(n + q)]), parity_of(n + q), &abort_flag);
+            return r;
+        };
+        auto release_parts = [&](int n, int parts) {
+            for (int q = 0; q < parts; ++q) mma_commit(smem_u32(&bars.empty[stage_of(n + q)]));
+        };
+        // D/16 k-steps of S (+)= A B^T with both operands [128 x D] tiles in shared memory
+        auto qk = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile, bool acc) {
+            const uint64_t ad = sdesc_sw128(a_tile, 16, 1024), bd = sdesc_sw128(b_tile, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = ((k >> 2) * C::DBLK + (k & 3) * 32) >> 4;
-                mma_ss(dst, qd + off, kd + off, C::IDESC_QK, k > 0);
+                mma_ss(dst, ad + off, bd + off, C::IDESC_QK, acc || k > 0);
             }
         };
-        // O_t (+)= P_t V; P_t is the bf16 copy over S_t's first 64 columns
-        auto issue_pv = [&](int t, int st, bool acc) {
-            const uint64_t vd = sdesc_sw128(sRing + st * C::TILE, C::DBLK, 1024);
+        // S_t = Q_t K^T for the K tile at stream position nk (x3: six part products)
+        auto issue_s = [&](int t, int nk) {
+            const uint32_t dst = tmem + (t ? C::S_COL1 : C::S_COL0);
+            auto qp = [&](int part) { return sQ + (2 * part + t) * C::TILE; };
+            auto kp = [&](int part) { return sRing + stage_of(nk + part) * C::TILE; };
+            qk(dst, qp(0), kp(0), false);
+            if constexpr (X3) {
+                qk(dst, qp(0), kp(1), true);
+                qk(dst, qp(1), kp(0), true);
+                qk(dst, qp(0), kp(2), true);
+                qk(dst, qp(2), kp(0), true);
+                qk(dst, qp(1), kp(1), true);
+            }
+        };
+        // k-steps of O (+)= P V: P (bf16) in TMEM from column pa, V tile at vd, N per idesc
+        auto pv = [&](uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, bool acc) {
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k) mma_ts(dst, pa + k * 8, vd + ((k * 2048) >> 4), idesc, acc || k > 0);
+        };
+        // O_t (+)= P_t V for the V tile at stream position nv; P_t is the bf16 copy over S_t's
+        // first 64 columns (x3: P hi there, P lo over the next 64)
+        auto issue_pv = [&](int t, int nv, bool acc) {
             const uint32_t dst = tmem + (t ? C::O_COL1 : C::O_COL0);
             const uint32_t pa = tmem + (t ? C::S_COL1 : C::S_COL0);
-#pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-                mma_ts(dst, pa + k * 8, vd + ((k * 2048) >> 4), C::IDESC_PV, acc || k > 0);
+            const uint32_t sv = stage_of(nv);
+            const uint64_t vd = sdesc_sw128(sRing + sv * C::TILE, C::DBLK, 1024);
+            if constexpr (!X3) {
+                pv(dst, pa, vd, C::IDESC_PV, acc);
+            } else {
+                const uint32_t sl = stage_of(nv + 1);
+                if (sl == sv + 1) {
+                    // Ph [Vh | Vl]: V lo is the next stage, one 64-column block on
+                    pv(dst, pa, vd, C::IDESC_PV2, acc);
+                } else {
+                    pv(dst, pa, vd, C::IDESC_PV, acc);
+                    pv(dst + D, pa, sdesc_sw128(sRing + sl * C::TILE, C::DBLK, 1024), C::IDESC_PV, acc);
+                }
+                pv(dst, pa + 64, vd, C::IDESC_PV, true);   // + Pl Vh into the first D columns
+            }
         };
         // PV for Q tile t at key tile i of an item; pc[t] counts P handshakes, oe[t] the O
         // hand-backs owed by earlier items
         int pc[2] = {0, 0}, oe[2] = {0, 0};
-        auto pv_step = [&](int t, int i, int nt, int sv) -> bool {
+        auto pv_step = [&](int t, int i, int nt, int nv) -> bool {
             if (i == 0 && oe[t] > 0 &&
                 !mbar_wait_spin(smem_u32(&bars.o_empty[t]), (oe[t] - 1) & 1, &abort_flag))
                 return false;
             if (!mbar_wait_spin(smem_u32(&bars.p_full[t]), pc[t] & 1, &abort_flag)) return false;
             ++pc[t];
             tc_fence_after();
-            issue_pv(t, sv, i > 0);
+            issue_pv(t, nv, i > 0);
             if (i == nt - 1) mma_commit(smem_u32(&bars.o_final[t]));
             return true;
         };
@@ -266,46 +342,46 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const int n0 = w.n0, n1 = w.n1, n_kv = w.n_kv;
             ok = mbar_wait_spin(smem_u32(&bars.q_full), qc & 1, &abort_flag);
             ++qc;
-            const int sk0 = stage_of(2 * gt);
-            if (ok) ok = mbar_wait_spin(smem_u32(&bars.full[sk0]), parity_of(2 * gt), &abort_flag);
+            const int nk0 = C::NPOS * gt;
+            if (ok) ok = wait_parts(nk0, C::KP);
             if (!ok) break;
             tc_fence_after();
             if (n0 > 0) {
-                issue_s(0, sk0);
+                issue_s(0, nk0);
                 mma_commit(smem_u32(&bars.s_full[0]));
             }
             if (n1 > 0) {
-                issue_s(1, sk0);
+                issue_s(1, nk0);
                 mma_commit(smem_u32(&bars.s_full[1]));
             }
-            mma_commit(smem_u32(&bars.empty[sk0]));
+            release_parts(nk0, C::KP);
             // Q is free once the item's last Q K^T products complete: the next item's Q tiles
             // then load while this item's last softmax and PV products run.
             if (n_kv == 1) mma_commit(smem_u32(&bars.q_empty));
             for (int i = 0; i < n_kv; ++i) {
-                const int nv = 2 * (gt + i) + 1, nk = 2 * (gt + i + 1);   // V_i and K_{i+1}
-                const int sv = stage_of(nv), sk = stage_of(nk);
+                // V_i and K_{i+1}
+                const int nv = C::NPOS * (gt + i) + C::KP, nk = C::NPOS * (gt + i + 1);
                 const bool more = i + 1 < n_kv;
-                ok = mbar_wait_spin(smem_u32(&bars.full[sv]), parity_of(nv), &abort_flag);
+                ok = wait_parts(nv, C::VP);
                 if (!ok) break;
-                if (i < n0 && !(ok = pv_step(0, i, n0, sv))) break;
+                if (i < n0 && !(ok = pv_step(0, i, n0, nv))) break;
                 if (more) {
-                    ok = mbar_wait_spin(smem_u32(&bars.full[sk]), parity_of(nk), &abort_flag);
+                    ok = wait_parts(nk, C::KP);
                     if (!ok) break;
                     tc_fence_after();
                     if (i + 1 < n0) {
-                        issue_s(0, sk);
+                        issue_s(0, nk);
                         mma_commit(smem_u32(&bars.s_full[0]));
                     }
                 }
-                if (i < n1 && !(ok = pv_step(1, i, n1, sv))) break;
-                mma_commit(smem_u32(&bars.empty[sv]));
+                if (i < n1 && !(ok = pv_step(1, i, n1, nv))) break;
+                release_parts(nv, C::VP);
                 if (more) {
                     if (i + 1 < n1) {
-                        issue_s(1, sk);
+                        issue_s(1, nk);
                         mma_commit(smem_u32(&bars.s_full[1]));
                     }
-                    mma_commit(smem_u32(&bars.empty[sk]));
+                    release_parts(nk, C::KP);
                     if (i + 2 == n_kv) mma_commit(smem_u32(&bars.q_empty));   // last Q K^T issued
                 }
             }
@@ -390,6 +466,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     acc[c] = f2_pack(0.f, 0.f);
+                    uint32_t pl[16];   // x3: the low bf16 part of P, p - bf16(p)
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
                         float p0, p1;
@@ -398,11 +475,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                         p0 = ex2_approx(p0);
                         p1 = ex2_approx(p1);
                         acc[c] = f2_add(acc[c], f2_pack(p0, p1));
-                        sr[c][k] = pack_bf16x2(p0, p1);
+                        const uint32_t ph = pack_bf16x2(p0, p1);
+                        sr[c][k] = ph;
+                        if constexpr (X3)
+                            pl[k] = pack_bf16x2(p0 - __uint_as_float(ph << 16), p1 - __uint_as_float(ph & 0xffff0000u));
                     }
                     tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
                               sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
                               sr[c][15]);
+                    // all 128 score columns are in registers, so P lo may overwrite columns 64..127
+                    if constexpr (X3)
+                        tmem_st16(s_addr + 64 + c * 16, pl[0], pl[1], pl[2], pl[3], pl[4], pl[5], pl[6], pl[7], pl[8],
+                                  pl[9], pl[10], pl[11], pl[12], pl[13], pl[14], pl[15]);
                 }
                 float rs;
                 {
@@ -417,7 +501,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     // waits for p_full, signalled below, after the rescaled O is stored.
                     const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < C::DO / 32; ++c) {
                         uint32_t o[32];
                         tmem_ld32(o_addr + c * 32, o);
                         tmem_ld_wait();
@@ -451,7 +535,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
                 const long long grow = (long long)w.bh * p.Sq + row;
                 const bool row_ok = row < p.Sq;
-                if (p.splits == 1) {
+                if (X3 && p.splits == 1) {
+                    // fp32 O = (O[:, :D] + O[:, D:]) / l
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    float *Og = static_cast<float *>(p.o) + o_at(p, w.b, w.hq, row);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t oa[32], ob[32];
+                        if (have_o) {
+                            tmem_ld32(o_addr + c * 32, oa);
+                            tmem_ld32(o_addr + D + c * 32, ob);
+                            tmem_ld_wait();
+                        }
+                        if (row_ok) {
+                            float4 *dst = reinterpret_cast<float4 *>(Og + c * 32);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                float v[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    v[e] = have_o ? (__uint_as_float(oa[4 * k + e]) + __uint_as_float(ob[4 * k + e])) * inv
+                                                  : 0.f;
+                                dst[k] = make_float4(v[0], v[1], v[2], v[3]);
+                            }
+                        }
+                    }
+                    if (p.lse && row_ok) p.lse[grow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                } else if (p.splits == 1) {
                     const float inv = l > 0.f ? 1.f / l : 0.f;
                     __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + o_at(p, w.b, w.hq, row);
                     // 32-byte stores when every row starts on a 32-byte boundary
@@ -489,6 +599,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                         uint32_t o[32];
                         if (have_o) {
                             tmem_ld32(o_addr + c * 32, o);
+                            if constexpr (X3) {
+                                uint32_t ob[32];
+                                tmem_ld32(o_addr + D + c * 32, ob);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int k = 0; k < 32; ++k)
+                                    o[k] = __float_as_uint(__uint_as_float(o[k]) + __uint_as_float(ob[k]));
+                            }
                             tmem_ld_wait();
                         }
                         if (row_ok) {
@@ -534,27 +652,107 @@ bool make_maps(const AttnProblem &p, CUtensorMap *mq, CUtensorMap *mk, CUtensorM
            make_bf16_tile_map_strided(mv, p.v, p.D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, BN);
 }
 
-template <int D>
-cudaError_t launch_t(const AttnProblem &p, int sm_count, cudaStream_t s) {
-    using C = TcCfg<D>;
+// x3 pre-pass: every float32 element of Q, K, V (any b/h/s strides) into its bf16 parts,
+// h = bf16(x), m = bf16(x - h), l = bf16(x - h - m), written as contiguous [B, H, S, D] arrays
+// Qh | Qm | Ql | Kh | Km | Kl | Vh | Vl (V keeps h and l = bf16(x - h)).  blockIdx.y selects
+// Q, K or V.
+__global__ void __launch_bounds__(256) split_parts_kernel(const AttnProblem p, __nv_bfloat16 *ws) {
+    const int which = blockIdx.y;
+    const int H = which == 0 ? p.Hq : p.Hkv;
+    const int S = which == 0 ? p.Sq : p.Sk;
+    const long long nq = (long long)p.B * p.Hq * p.Sq * p.D, nk = (long long)p.B * p.Hkv * p.Sk * p.D;
+    const long long n = which == 0 ? nq : nk;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int d = (int)(i % p.D);
+    long long r = i / p.D;
+    const long long sidx = r % S;
+    r /= S;
+    const int h = (int)(r % H), b = (int)(r / H);
+    float x;
+    __nv_bfloat16 *out;
+    if (which == 0) {
+        x = static_cast<const float *>(p.q)[q_at(p, b, h, sidx) + d];
+        out = ws;
+    } else if (which == 1) {
+        x = static_cast<const float *>(p.k)[k_at(p, b, h, sidx) + d];
+        out = ws + 3 * nq;
+    } else {
+        x = static_cast<const float *>(p.v)[v_at(p, b, h, sidx) + d];
+        out = ws + 3 * nq + 3 * nk;
+    }
+    const __nv_bfloat16 h16 = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(h16);
+    out[i] = h16;
+    if (which == 2) {
+        out[i + n] = __float2bfloat16_rn(r1);
+    } else {
+        const __nv_bfloat16 m16 = __float2bfloat16_rn(r1);
+        out[i + n] = m16;
+        out[i + 2 * n] = __float2bfloat16_rn(r1 - __bfloat162float(m16));
+    }
+}
+
+template <int D, bool X3>
+cudaError_t launch_t(const AttnProblem &p, const CUtensorMap (&m)[8], int sm_count, cudaStream_t s) {
+    using C = TcCfg<D, X3>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, X3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap mq, mk, mv;
-    if (!make_maps(p, &mq, &mk, &mv)) return cudaErrorInvalidValue;
     const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
     const long long items = (long long)n_qb * p.B * p.Hq;
     if (items >= (1LL << 31)) return cudaErrorInvalidValue;
     // one resident CTA per SM walks the items; fewer items than SMs: one CTA per item
     const int grid = (int)(items < sm_count ? items : (sm_count > 0 ? sm_count : 1));
-    attn_tc_kernel<D><<<dim3((unsigned)grid, (unsigned)p.splits), NTHREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p, n_qb,
-                                                                                                 (int)items);
+    attn_tc_kernel<D, X3><<<dim3((unsigned)grid, (unsigned)p.splits), NTHREADS, C::SMEM_BYTES, s>>>(
+        m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p, n_qb, (int)items);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// bf16 inputs: maps on the caller's tensors (the part maps are unused copies).
+cudaError_t launch_bf16(const AttnProblem &p, int sm_count, cudaStream_t s) {
+    CUtensorMap m[8];
+    if (!make_maps(p, &m[0], &m[1], &m[2])) return cudaErrorInvalidValue;
+    m[3] = m[6] = m[0];
+    m[4] = m[7] = m[1];
+    m[5] = m[2];
+    return p.D == 64 ? launch_t<64, false>(p, m, sm_count, s) : launch_t<128, false>(p, m, sm_count, s);
+}
+
+// float32 inputs (D = 64): split Q, K, V into bf16 parts in the workspace, then run x3 mode on
+// contiguous maps of the parts.  Map order: Qh Kh Vh Qm Km Ql Kl Vl.
+cudaError_t launch_x3(const AttnProblem &p, int sm_count, cudaStream_t s) {
+    const long long nq = (long long)p.B * p.Hq * p.Sq * p.D, nk = (long long)p.B * p.Hkv * p.Sk * p.D;
+    __nv_bfloat16 *ws = static_cast<__nv_bfloat16 *>(p.x3_ws);
+    if (!ws) return cudaErrorInvalidValue;
+    const long long nmax = nq > nk ? nq : nk;
+    const long long blocks = (nmax + 255) / 256;
+    if (blocks >= (1LL << 31)) return cudaErrorInvalidValue;
+    split_parts_kernel<<<dim3((unsigned)blocks, 3), 256, 0, s>>>(p, ws);
+    count_launches(1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const __nv_bfloat16 *q[3] = {ws, ws + nq, ws + 2 * nq};
+    const __nv_bfloat16 *k[3] = {ws + 3 * nq, ws + 3 * nq + nk, ws + 3 * nq + 2 * nk};
+    const __nv_bfloat16 *v[2] = {ws + 3 * nq + 3 * nk, ws + 3 * nq + 4 * nk};
+    const int D = p.D;
+    const long long qs = (long long)p.Sq * D, ks = (long long)p.Sk * D;
+    auto qmap = [&](CUtensorMap *m, const void *g) {
+        return make_bf16_tile_map_strided(m, g, D, p.Sq, p.Hq, p.B, D, qs, qs * p.Hq, BM);
+    };
+    auto kmap = [&](CUtensorMap *m, const void *g) {
+        return make_bf16_tile_map_strided(m, g, D, p.Sk, p.Hkv, p.B, D, ks, ks * p.Hkv, BN);
+    };
+    CUtensorMap m[8];
+    if (!qmap(&m[0], q[0]) || !kmap(&m[1], k[0]) || !kmap(&m[2], v[0]) || !qmap(&m[3], q[1]) ||
+        !kmap(&m[4], k[1]) || !qmap(&m[5], q[2]) || !kmap(&m[6], k[2]) || !kmap(&m[7], v[1]))
+        return cudaErrorInvalidValue;
+    return launch_t<64, true>(p, m, sm_count, s);
 }
 
 // CTAs the kernel runs for a problem (before any key split).
@@ -565,6 +763,12 @@ long long tc_ctas(const AttnProblem &p) {
 }  // namespace
 
 bool attn_tc_supported(const AttnProblem &p, const void *Q, const void *K, const void *V, const void *O) {
+    if (p.dtype == OSF_F32) {
+        // x3 mode: the pre-pass reads Q, K, V with any strides; the epilogue stores 16-byte
+        // pieces of each fp32 O row
+        if (p.Sq < 2 || p.D != 64 || !aligned16(O) || ((p.o_ss | p.o_sh | p.o_sb) * 4) % 16 != 0) return false;
+        return tc_ctas(p) < (1LL << 31) && tensor_map_encoder() != nullptr;
+    }
     if (p.dtype != OSF_BF16 || p.Sq < 2 || (p.D != 64 && p.D != 128)) return false;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return false;
     // the epilogue stores 16-byte pieces of each O row
@@ -574,6 +778,12 @@ bool attn_tc_supported(const AttnProblem &p, const void *Q, const void *K, const
            tile_map_addressable(p.q, p.D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb) &&
            tile_map_addressable(p.k, p.D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb) &&
            tile_map_addressable(p.v, p.D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb);
+}
+
+size_t attn_tc_extra_bytes(const AttnProblem &p) {
+    if (p.dtype != OSF_F32) return 0;
+    const size_t nq = (size_t)p.B * p.Hq * p.Sq * p.D, nk = (size_t)p.B * p.Hkv * p.Sk * p.D;
+    return 2 * (3 * nq + 5 * nk);   // bf16 parts: three of Q and K, two of V
 }
 
 int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {
@@ -587,7 +797,7 @@ int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {
 }
 
 cudaError_t launch_attn_tc(const AttnProblem &p, int sm_count, cudaStream_t s) {
-    cudaError_t e = p.D == 64 ? launch_t<64>(p, sm_count, s) : launch_t<128>(p, sm_count, s);
+    cudaError_t e = p.dtype == OSF_F32 ? launch_x3(p, sm_count, s) : launch_bf16(p, sm_count, s);
     if (e == cudaSuccess && p.splits > 1) e = launch_attn_combine(p, s);
     return e;
 }

@@ -68,6 +68,7 @@ struct AttnProblem {
     // split-K partial state workspace (float): acc [splits][B*Hq*Sq][D], m/l [splits][B*Hq*Sq]
     int splits;
     float *part_acc, *part_m, *part_l;
+    void *x3_ws;         // fp32 on the tensor-core path: bf16 high / low parts of Q, K, V
     int *status;         // device status word
 };
 
