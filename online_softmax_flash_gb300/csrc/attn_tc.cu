@@ -261,15 +261,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         // (>> 4) to the start-address field, which cannot carry out of its 14 bits because
         // shared-memory addresses stay below 256 KiB.
         // Stream positions of key tile g: K parts from NPOS*g, V parts from NPOS*g + KP.  An
-        // operand's parts are waited for and released together.
-        auto wait_parts = [&](int n, int parts) {
-            bool r = true;
-            for (int q = 0; q < parts && r; ++q)
-                r = mbar_wait_spin(smem_u32(&bars.full[stage_of(n + q)]), parity_of(n + q), &abort_flag);
+        // operand's parts (consecutive positions from stage st, parity ph) are waited for and
+        // released together.  Stages and parities are computed before the waits: anything
+        // between a wait and the MMAs it releases lengthens the P hand-off chain.
+        // the stage after stage s (the parity flips when the ring wraps)
+        auto next_stage = [](int s) { return s + 1 == C::STAGES ? 0 : s + 1; };
+        auto wait_parts = [&](int st, uint32_t ph, int parts) {
+            bool r = mbar_wait_spin(smem_u32(&bars.full[st]), ph, &abort_flag);
+            for (int q = 1; q < parts && r; ++q) {
+                st = next_stage(st);
+                if (st == 0) ph ^= 1;
+                r = mbar_wait_spin(smem_u32(&bars.full[st]), ph, &abort_flag);
+            }
             return r;
         };
-        auto release_parts = [&](int n, int parts) {
-            for (int q = 0; q < parts; ++q) mma_commit(smem_u32(&bars.empty[stage_of(n + q)]));
+        auto release_parts = [&](int st, int parts) {
+            mma_commit(smem_u32(&bars.empty[st]));
+            for (int q = 1; q < parts; ++q) {
+                st = next_stage(st);
+                mma_commit(smem_u32(&bars.empty[st]));
+            }
         };
         // D/16 k-steps of S (+)= A B^T with both operands [128 x D] tiles in shared memory
         auto qk = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile, bool acc) {
@@ -280,18 +291,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 mma_ss(dst, ad + off, bd + off, C::IDESC_QK, acc || k > 0);
             }
         };
-        // S_t = Q_t K^T for the K tile at stream position nk (x3: six part products)
-        auto issue_s = [&](int t, int nk) {
+        // S_t = Q_t K^T for the K tile (first part) in stage k0 (x3: six part products)
+        auto issue_s = [&](int t, int k0) {
             const uint32_t dst = tmem + (t ? C::S_COL1 : C::S_COL0);
             auto qp = [&](int part) { return sQ + (2 * part + t) * C::TILE; };
-            auto kp = [&](int part) { return sRing + stage_of(nk + part) * C::TILE; };
-            qk(dst, qp(0), kp(0), false);
+            qk(dst, qp(0), sRing + k0 * C::TILE, false);
             if constexpr (X3) {
-                qk(dst, qp(0), kp(1), true);
-                qk(dst, qp(1), kp(0), true);
-                qk(dst, qp(0), kp(2), true);
-                qk(dst, qp(2), kp(0), true);
-                qk(dst, qp(1), kp(1), true);
+                const int k1 = next_stage(k0), k2 = next_stage(k1);
+                const uint32_t kh = sRing + k0 * C::TILE, km = sRing + k1 * C::TILE, kl = sRing + k2 * C::TILE;
+                qk(dst, qp(0), km, true);
+                qk(dst, qp(1), kh, true);
+                qk(dst, qp(0), kl, true);
+                qk(dst, qp(2), kh, true);
+                qk(dst, qp(1), km, true);
             }
         };
         // k-steps of O (+)= P V: P (bf16) in TMEM from column pa, V tile at vd, N per idesc
@@ -299,17 +311,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
             for (int k = 0; k < BN / 16; ++k) mma_ts(dst, pa + k * 8, vd + ((k * 2048) >> 4), idesc, acc || k > 0);
         };
-        // O_t (+)= P_t V for the V tile at stream position nv; P_t is the bf16 copy over S_t's
+        // O_t (+)= P_t V for the V tile (first part) in stage sv; P_t is the bf16 copy over S_t's
         // first 64 columns (x3: P hi there, P lo over the next 64)
-        auto issue_pv = [&](int t, int nv, bool acc) {
+        auto issue_pv = [&](int t, int sv, bool acc) {
             const uint32_t dst = tmem + (t ? C::O_COL1 : C::O_COL0);
             const uint32_t pa = tmem + (t ? C::S_COL1 : C::S_COL0);
-            const uint32_t sv = stage_of(nv);
             const uint64_t vd = sdesc_sw128(sRing + sv * C::TILE, C::DBLK, 1024);
             if constexpr (!X3) {
                 pv(dst, pa, vd, C::IDESC_PV, acc);
             } else {
-                const uint32_t sl = stage_of(nv + 1);
+                const int sl = next_stage(sv);
                 if (sl == sv + 1) {
                     // Ph [Vh | Vl]: V lo is the next stage, one 64-column block on
                     pv(dst, pa, vd, C::IDESC_PV2, acc);
@@ -323,14 +334,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         // PV for Q tile t at key tile i of an item; pc[t] counts P handshakes, oe[t] the O
         // hand-backs owed by earlier items
         int pc[2] = {0, 0}, oe[2] = {0, 0};
-        auto pv_step = [&](int t, int i, int nt, int nv) -> bool {
+        auto pv_step = [&](int t, int i, int nt, int sv) -> bool {
             if (i == 0 && oe[t] > 0 &&
                 !mbar_wait_spin(smem_u32(&bars.o_empty[t]), (oe[t] - 1) & 1, &abort_flag))
                 return false;
             if (!mbar_wait_spin(smem_u32(&bars.p_full[t]), pc[t] & 1, &abort_flag)) return false;
             ++pc[t];
             tc_fence_after();
-            issue_pv(t, nv, i > 0);
+            issue_pv(t, sv, i > 0);
             if (i == nt - 1) mma_commit(smem_u32(&bars.o_final[t]));
             return true;
         };
@@ -342,46 +353,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const int n0 = w.n0, n1 = w.n1, n_kv = w.n_kv;
             ok = mbar_wait_spin(smem_u32(&bars.q_full), qc & 1, &abort_flag);
             ++qc;
-            const int nk0 = C::NPOS * gt;
-            if (ok) ok = wait_parts(nk0, C::KP);
+            const int sk0 = stage_of(C::NPOS * gt);
+            if (ok) ok = wait_parts(sk0, parity_of(C::NPOS * gt), C::KP);
             if (!ok) break;
             tc_fence_after();
             if (n0 > 0) {
-                issue_s(0, nk0);
+                issue_s(0, sk0);
                 mma_commit(smem_u32(&bars.s_full[0]));
             }
             if (n1 > 0) {
-                issue_s(1, nk0);
+                issue_s(1, sk0);
                 mma_commit(smem_u32(&bars.s_full[1]));
             }
-            release_parts(nk0, C::KP);
+            release_parts(sk0, C::KP);
             // Q is free once the item's last Q K^T products complete: the next item's Q tiles
             // then load while this item's last softmax and PV products run.
             if (n_kv == 1) mma_commit(smem_u32(&bars.q_empty));
             for (int i = 0; i < n_kv; ++i) {
                 // V_i and K_{i+1}
                 const int nv = C::NPOS * (gt + i) + C::KP, nk = C::NPOS * (gt + i + 1);
+                const int sv = stage_of(nv), sk = stage_of(nk);
+                const uint32_t phv = parity_of(nv), phk = parity_of(nk);
                 const bool more = i + 1 < n_kv;
-                ok = wait_parts(nv, C::VP);
+                ok = wait_parts(sv, phv, C::VP);
                 if (!ok) break;
-                if (i < n0 && !(ok = pv_step(0, i, n0, nv))) break;
+                if (i < n0 && !(ok = pv_step(0, i, n0, sv))) break;
                 if (more) {
-                    ok = wait_parts(nk, C::KP);
+                    ok = wait_parts(sk, phk, C::KP);
                     if (!ok) break;
                     tc_fence_after();
                     if (i + 1 < n0) {
-                        issue_s(0, nk);
+                        issue_s(0, sk);
                         mma_commit(smem_u32(&bars.s_full[0]));
                     }
                 }
-                if (i < n1 && !(ok = pv_step(1, i, n1, nv))) break;
-                release_parts(nv, C::VP);
+                if (i < n1 && !(ok = pv_step(1, i, n1, sv))) break;
+                release_parts(sv, C::VP);
                 if (more) {
                     if (i + 1 < n1) {
-                        issue_s(1, nk);
+                        issue_s(1, sk);
                         mma_commit(smem_u32(&bars.s_full[1]));
                     }
-                    release_parts(nk, C::KP);
+                    release_parts(sk, C::KP);
                     if (i + 2 == n_kv) mma_commit(smem_u32(&bars.q_empty));   // last Q K^T issued
                 }
             }
