@@ -49,6 +49,9 @@ constexpr uint32_t TMEM_COLS = 512;
 // about 88 registers that happened.  128*104 + 256*200 = 384*168, the registers the CTA is
 // launched with (168 per thread).
 constexpr int kCtrlRegs = 88, kSoftmaxRegs = 208;
+// x3 mode: the issuer carries six score products per tile and the softmax holds one chunk at a
+// time: 128*120 + 256*192 = 384*168 as well
+constexpr int kCtrlRegsX3 = 120, kSoftmaxRegsX3 = 192;
 constexpr float kRescaleThreshold = 8.0f;   // base-2 units
 
 constexpr uint32_t kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KiB)
@@ -193,7 +196,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     const uint32_t tmem = tmem_base_sh;
 
     if (warp < 4) {
-      setmaxnreg_dec<kCtrlRegs>();
+      setmaxnreg_dec<X3 ? kCtrlRegsX3 : kCtrlRegs>();
       if ((warp == 0 || warp == 2) && lane == 0) {
         // ============================================================== TMA producers
         // The ring receives K V K V ... in consumption order; warp 0 issues the Q tiles and the
@@ -311,6 +314,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
             for (int k = 0; k < BN / 16; ++k) mma_ts(dst, pa + k * 8, vd + ((k * 2048) >> 4), idesc, acc || k > 0);
         };
+        // x3 layout: keys 32c..32c+31 of a P part sit in columns 32c + [0, 16) (hi) or + [16, 32)
+        // (lo); k-step k (16 keys) starts at column 32 (k / 2) + 8 (k % 2) from the part's base
+        auto pv_x3 = [&](uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, bool acc) {
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+                mma_ts(dst, pa + 32 * (k >> 1) + 8 * (k & 1), vd + ((k * 2048) >> 4), idesc, acc || k > 0);
+        };
         // O_t (+)= P_t V for the V tile (first part) in stage sv; P_t is the bf16 copy over S_t's
         // first 64 columns (x3: P hi there, P lo over the next 64)
         auto issue_pv = [&](int t, int sv, bool acc) {
@@ -323,12 +333,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 const int sl = next_stage(sv);
                 if (sl == sv + 1) {
                     // Ph [Vh | Vl]: V lo is the next stage, one 64-column block on
-                    pv(dst, pa, vd, C::IDESC_PV2, acc);
+                    pv_x3(dst, pa, vd, C::IDESC_PV2, acc);
                 } else {
-                    pv(dst, pa, vd, C::IDESC_PV, acc);
-                    pv(dst + D, pa, sdesc_sw128(sRing + sl * C::TILE, C::DBLK, 1024), C::IDESC_PV, acc);
+                    pv_x3(dst, pa, vd, C::IDESC_PV, acc);
+                    pv_x3(dst + D, pa, sdesc_sw128(sRing + sl * C::TILE, C::DBLK, 1024), C::IDESC_PV, acc);
                 }
-                pv(dst, pa + 64, vd, C::IDESC_PV, true);   // + Pl Vh into the first D columns
+                pv_x3(dst, pa + 16, vd, C::IDESC_PV, true);   // + Pl Vh into the first D columns
             }
         };
         // PV for Q tile t at key tile i of an item; pc[t] counts P handshakes, oe[t] the O
@@ -409,7 +419,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
       }
     } else {
-        setmaxnreg_inc<kSoftmaxRegs>();
+        setmaxnreg_inc<X3 ? kSoftmaxRegsX3 : kSoftmaxRegs>();
         // ============================================================== softmax
         const int t = (warp - 4) >> 2;           // Q tile
         const int r = tid - 128 * (t + 1);       // row within the tile == TMEM lane
@@ -432,34 +442,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (!ok) break;
                 ++sc;
                 tc_fence_after();
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-                tmem_ld_wait();
                 const int key0 = (w.kt_begin + i) * BN;
                 const bool need_mask = (key0 + BN > p.Sk) || (p.causal && key0 + BN - 1 > row_first + p.causal_off);
-                if (need_mask) {
-                    // column j of the tile (key key0 + j) is kept iff j < lim: inside the sequence
-                    // and, when causal, not after the last key this row sees
-                    int lim = p.Sk - key0;
-                    if (p.causal) lim = min(lim, row + p.causal_off - key0 + 1);
+                // column j of the tile (key key0 + j) is kept iff j < lim: inside the sequence
+                // and, when causal, not after the last key this row sees
+                int lim = p.Sk - key0;
+                if (p.causal) lim = min(lim, row + p.causal_off - key0 + 1);
+                uint32_t sr[X3 ? 1 : 4][32];   // bf16 mode: the whole score row in registers
+                float mx;
+                if constexpr (X3) {
+                    // two passes over TMEM (the row max, then P) keep one 32-column chunk in
+                    // registers, which leaves room for P's two parts
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(s_addr + c * 32, sr[0]);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                        for (int k = 0; k < 32; ++k) {
+                            const float x = (need_mask && c * 32 + k >= lim) ? -INFINITY : __uint_as_float(sr[0][k]);
+                            m4[k & 3] = fmaxf(m4[k & 3], x);
+                        }
+                    }
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                } else {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (c * 32 + k >= lim) sr[c][k] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+                    tmem_ld_wait();
+                    if (need_mask) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (c * 32 + k >= lim) sr[c][k] = __float_as_uint(-INFINITY);
+                    }
+                    // row max: eight independent chains of 3-input max, then a short tree
+                    float mm[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int c = g >> 1, k0 = (g & 1) * 16;
+                        mm[g] = fmaxf(__uint_as_float(sr[c][k0]), __uint_as_float(sr[c][k0 + 1]));
+#pragma unroll
+                        for (int v = 1; v < 8; ++v)
+                            mm[g] = fmax3(mm[g], __uint_as_float(sr[c][k0 + 2 * v]), __uint_as_float(sr[c][k0 + 2 * v + 1]));
+                    }
+                    mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[7]));
                 }
-                // row max: eight independent chains of 3-input max, then a short tree
-                float mm[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const int c = g >> 1, k0 = (g & 1) * 16;
-                    mm[g] = fmaxf(__uint_as_float(sr[c][k0]), __uint_as_float(sr[c][k0 + 1]));
-#pragma unroll
-                    for (int v = 1; v < 8; ++v)
-                        mm[g] = fmax3(mm[g], __uint_as_float(sr[c][k0 + 2 * v]), __uint_as_float(sr[c][k0 + 2 * v + 1]));
-                }
-                const float mx = fmax3(fmax3(mm[0], mm[1], mm[2]), fmax3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[7]));
                 const float m_tile = mx * sl2;   // -inf stays -inf (sl2 > 0)
                 const float m_new = fmaxf(m_ref, m_tile);
                 const bool rescale = __any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold);
@@ -473,36 +501,59 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
                 const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
                 const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mr, -mr);
-                uint64_t acc[4];
-                // p = 2^(s * scale * log2e - m): pairs through one f32x2 FMA, sums in four
-                // independent f32x2 accumulators; P packed to bf16 over the first half of S.
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    acc[c] = f2_pack(0.f, 0.f);
-                    uint32_t pl[16];   // x3: the low bf16 part of P, p - bf16(p)
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float p0, p1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * k]), __uint_as_float(sr[c][2 * k + 1])), sc2, nm2),
-                                  p0, p1);
-                        p0 = ex2_approx(p0);
-                        p1 = ex2_approx(p1);
-                        acc[c] = f2_add(acc[c], f2_pack(p0, p1));
-                        const uint32_t ph = pack_bf16x2(p0, p1);
-                        sr[c][k] = ph;
-                        if constexpr (X3)
-                            pl[k] = pack_bf16x2(p0 - __uint_as_float(ph << 16), p1 - __uint_as_float(ph & 0xffff0000u));
-                    }
-                    tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
-                              sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
-                              sr[c][15]);
-                    // all 128 score columns are in registers, so P lo may overwrite columns 64..127
-                    if constexpr (X3)
-                        tmem_st16(s_addr + 64 + c * 16, pl[0], pl[1], pl[2], pl[3], pl[4], pl[5], pl[6], pl[7], pl[8],
-                                  pl[9], pl[10], pl[11], pl[12], pl[13], pl[14], pl[15]);
-                }
                 float rs;
-                {
+                if constexpr (X3) {
+                    // chunk c (keys 32c..32c+31) puts P hi over its own first 16 columns and
+                    // P lo = bf16(p - P hi) over its last 16, so no chunk overwrites unread scores
+                    uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(s_addr + c * 32, sr[0]);
+                        tmem_ld_wait();
+                        uint32_t ph[16], pl[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float s0 = (need_mask && c * 32 + 2 * k >= lim) ? -INFINITY : __uint_as_float(sr[0][2 * k]);
+                            const float s1 = (need_mask && c * 32 + 2 * k + 1 >= lim) ? -INFINITY
+                                                                                     : __uint_as_float(sr[0][2 * k + 1]);
+                            float p0, p1;
+                            f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), p0, p1);
+                            p0 = ex2_approx(p0);
+                            p1 = ex2_approx(p1);
+                            acc = f2_add(acc, f2_pack(p0, p1));
+                            ph[k] = pack_bf16x2(p0, p1);
+                            pl[k] = pack_bf16x2(p0 - __uint_as_float(ph[k] << 16), p1 - __uint_as_float(ph[k] & 0xffff0000u));
+                        }
+                        tmem_st16(s_addr + c * 32, ph[0], ph[1], ph[2], ph[3], ph[4], ph[5], ph[6], ph[7], ph[8], ph[9],
+                                  ph[10], ph[11], ph[12], ph[13], ph[14], ph[15]);
+                        tmem_st16(s_addr + c * 32 + 16, pl[0], pl[1], pl[2], pl[3], pl[4], pl[5], pl[6], pl[7], pl[8],
+                                  pl[9], pl[10], pl[11], pl[12], pl[13], pl[14], pl[15]);
+                    }
+                    float lo, hi;
+                    f2_unpack(acc, lo, hi);
+                    rs = lo + hi;
+                } else {
+                    uint64_t acc[4];
+                    // p = 2^(s * scale * log2e - m): pairs through one f32x2 FMA, sums in four
+                    // independent f32x2 accumulators; P packed to bf16 over the first half of S.
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[c] = f2_pack(0.f, 0.f);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            float p0, p1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * k]), __uint_as_float(sr[c][2 * k + 1])),
+                                             sc2, nm2),
+                                      p0, p1);
+                            p0 = ex2_approx(p0);
+                            p1 = ex2_approx(p1);
+                            acc[c] = f2_add(acc[c], f2_pack(p0, p1));
+                            sr[c][k] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
+                                  sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
+                                  sr[c][15]);
+                    }
                     const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
                     float lo, hi;
                     f2_unpack(a2, lo, hi);
