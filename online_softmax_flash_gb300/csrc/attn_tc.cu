@@ -718,42 +718,61 @@ bool make_maps(const AttnProblem &p, CUtensorMap *mq, CUtensorMap *mk, CUtensorM
 
 // x3 pre-pass: every float32 element of Q, K, V (any b/h/s strides) into its bf16 parts,
 // h = bf16(x), m = bf16(x - h), l = bf16(x - h - m), written as contiguous [B, H, S, D] arrays
-// Qh | Qm | Ql | Kh | Km | Kl | Vh | Vl (V keeps h and l = bf16(x - h)).  blockIdx.y selects
-// Q, K or V.
+// Qh | Qm | Ql | Kh | Km | Kl | Vh | Vl (V keeps h and l = bf16(x - h), the "m" slot).
+// blockIdx.y selects Q, K or V.
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// One thread per four consecutive elements of a row (D = 64: 16 threads per row).
 __global__ void __launch_bounds__(256) split_parts_kernel(const AttnProblem p, __nv_bfloat16 *ws) {
     const int which = blockIdx.y;
     const int H = which == 0 ? p.Hq : p.Hkv;
     const int S = which == 0 ? p.Sq : p.Sk;
     const long long nq = (long long)p.B * p.Hq * p.Sq * p.D, nk = (long long)p.B * p.Hkv * p.Sk * p.D;
     const long long n = which == 0 ? nq : nk;
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const int d = (int)(i % p.D);
-    long long r = i / p.D;
-    const long long sidx = r % S;
-    r /= S;
-    const int h = (int)(r % H), b = (int)(r / H);
-    float x;
+    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of 4 elements
+    if (g * 4 >= n) return;
+    const int per_row = p.D >> 2;
+    const long long row = g / per_row;
+    const int d = (int)(g - row * per_row) * 4;
+    const long long sidx = row % S;
+    const long long bh = row / S;
+    const int h = (int)(bh % H), b = (int)(bh / H);
+    const float *src;
     __nv_bfloat16 *out;
     if (which == 0) {
-        x = static_cast<const float *>(p.q)[q_at(p, b, h, sidx) + d];
+        src = static_cast<const float *>(p.q) + q_at(p, b, h, sidx) + d;
         out = ws;
     } else if (which == 1) {
-        x = static_cast<const float *>(p.k)[k_at(p, b, h, sidx) + d];
+        src = static_cast<const float *>(p.k) + k_at(p, b, h, sidx) + d;
         out = ws + 3 * nq;
     } else {
-        x = static_cast<const float *>(p.v)[v_at(p, b, h, sidx) + d];
+        src = static_cast<const float *>(p.v) + v_at(p, b, h, sidx) + d;
         out = ws + 3 * nq + 3 * nk;
     }
-    const __nv_bfloat16 h16 = __float2bfloat16_rn(x);
-    const float r1 = x - __bfloat162float(h16);
-    out[i] = h16;
-    if (which == 2) {
-        out[i + n] = __float2bfloat16_rn(r1);
+    float x[4];
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     } else {
-        const __nv_bfloat16 m16 = __float2bfloat16_rn(r1);
-        out[i + n] = m16;
-        out[i + 2 * n] = __float2bfloat16_rn(r1 - __bfloat162float(m16));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = src[e];
+    }
+    const long long i = row * p.D + d;   // element index in the contiguous part arrays
+    // h = bf16(x), m = bf16(x - h), l = bf16(x - h - m)
+    const uint32_t h01 = bf16_pair(x[0], x[1]), h23 = bf16_pair(x[2], x[3]);
+    const float r[4] = {x[0] - bf16_lo(h01), x[1] - bf16_hi(h01), x[2] - bf16_lo(h23), x[3] - bf16_hi(h23)};
+    const uint32_t m01 = bf16_pair(r[0], r[1]), m23 = bf16_pair(r[2], r[3]);
+    *reinterpret_cast<uint2 *>(out + i) = make_uint2(h01, h23);
+    *reinterpret_cast<uint2 *>(out + i + n) = make_uint2(m01, m23);
+    if (which != 2) {
+        const uint32_t l01 = bf16_pair(r[0] - bf16_lo(m01), r[1] - bf16_hi(m01));
+        const uint32_t l23 = bf16_pair(r[2] - bf16_lo(m23), r[3] - bf16_hi(m23));
+        *reinterpret_cast<uint2 *>(out + i + 2 * n) = make_uint2(l01, l23);
     }
 }
 
@@ -795,7 +814,7 @@ cudaError_t launch_x3(const AttnProblem &p, int sm_count, cudaStream_t s) {
     __nv_bfloat16 *ws = static_cast<__nv_bfloat16 *>(p.x3_ws);
     if (!ws) return cudaErrorInvalidValue;
     const long long nmax = nq > nk ? nq : nk;
-    const long long blocks = (nmax + 255) / 256;
+    const long long blocks = (nmax / 4 + 255) / 256;   // one thread per four elements (D % 4 == 0)
     if (blocks >= (1LL << 31)) return cudaErrorInvalidValue;
     split_parts_kernel<<<dim3((unsigned)blocks, 3), 256, 0, s>>>(p, ws);
     count_launches(1);
