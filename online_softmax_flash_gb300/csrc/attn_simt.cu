@@ -217,6 +217,7 @@ attn_simt_kernel(const AttnProblem p) {
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) {
     constexpr int SG = 8;   // splits per load group
+    griddep_wait();   // launched as a dependent of the kernel that wrote the partial states
     const long long rows_total = (long long)p.B * p.Hq * p.Sq;
     const int groups = (p.D + 3) >> 2;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -329,13 +330,14 @@ cudaError_t launch_attn_combine(const AttnProblem &p, cudaStream_t s) {
     const long long threads = rows_total * ((p.D + 3) / 4);
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     const bool vec = p.D % 4 == 0;   // part_acc rows are then 16-byte aligned
-    if (p.dtype == OSF_F32) {
-        if (vec) attn_combine_kernel<float, true><<<blocks, 256, 0, s>>>(p);
-        else attn_combine_kernel<float, false><<<blocks, 256, 0, s>>>(p);
-    } else {
-        if (vec) attn_combine_kernel<__nv_bfloat16, true><<<blocks, 256, 0, s>>>(p);
-        else attn_combine_kernel<__nv_bfloat16, false><<<blocks, 256, 0, s>>>(p);
-    }
+    cudaError_t e;
+    if (p.dtype == OSF_F32)
+        e = launch_dependent(vec ? attn_combine_kernel<float, true> : attn_combine_kernel<float, false>, dim3(blocks),
+                             dim3(256), 0, s, p);
+    else
+        e = launch_dependent(vec ? attn_combine_kernel<__nv_bfloat16, true> : attn_combine_kernel<__nv_bfloat16, false>,
+                             dim3(blocks), dim3(256), 0, s, p);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -198,6 +198,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     if (warp < 4) {
       setmaxnreg_dec<X3 ? kCtrlRegsX3 : kCtrlRegs>();
       if ((warp == 0 || warp == 2) && lane == 0) {
+        // float32 mode runs as a dependent of the split pre-pass: its parts are read by TMA only
+        if (X3) griddep_wait();
         // ============================================================== TMA producers
         // The ring receives K V K V ... in consumption order; warp 0 issues the Q tiles and the
         // K tiles (even stream positions), warp 2 the V tiles (odd positions), one TMA
@@ -791,8 +793,16 @@ cudaError_t launch_t(const AttnProblem &p, const CUtensorMap (&m)[8], int sm_cou
     if (items >= (1LL << 31)) return cudaErrorInvalidValue;
     // one resident CTA per SM walks the items; fewer items than SMs: one CTA per item
     const int grid = (int)(items < sm_count ? items : (sm_count > 0 ? sm_count : 1));
-    attn_tc_kernel<D, X3><<<dim3((unsigned)grid, (unsigned)p.splits), NTHREADS, C::SMEM_BYTES, s>>>(
-        m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p, n_qb, (int)items);
+    const dim3 g((unsigned)grid, (unsigned)p.splits);
+    if (X3) {
+        // dependent of the split pre-pass (see the producers' griddep_wait)
+        cudaError_t e = launch_dependent(attn_tc_kernel<D, X3>, g, dim3(NTHREADS), C::SMEM_BYTES, s, m[0], m[1], m[2],
+                                         m[3], m[4], m[5], m[6], m[7], p, n_qb, (int)items);
+        if (e != cudaSuccess) return e;
+    } else {
+        attn_tc_kernel<D, X3><<<g, NTHREADS, C::SMEM_BYTES, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p,
+                                                                  n_qb, (int)items);
+    }
     count_launches(1);
     return cudaGetLastError();
 }

@@ -18,6 +18,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kStatusTimeout = OSF_ERR_TIMEOUT;
 
 // ---------------------------------------------------------------- device helpers
+// Wait until the grid this kernel was launched as a programmatic dependent of has completed and
+// its memory is visible (a no-op for a kernel launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -88,6 +92,26 @@ __host__ __device__ __forceinline__ long long o_at(const AttnProblem &p, int b, 
 
 // Count of kernels launched by the library (diagnostics; see osf_launch_count).
 void count_launches(int n);
+
+// Launch `kernel` as a programmatic dependent of the previous kernel in the stream: it is
+// scheduled as soon as every block of that kernel has finished, without the launch gap, and
+// must execute griddepcontrol.wait before it reads anything that kernel wrote (the wait returns
+// once the previous grid has completed and its memory operations are visible).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t s);
