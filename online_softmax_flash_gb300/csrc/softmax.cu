@@ -182,6 +182,7 @@ template <bool VEC4>
 __global__ void __launch_bounds__(kChunkThreads)
 softmax_chunk_norm_kernel(const float *x, float *z, long long T, long long chunk,
                           const float2 *__restrict__ ws) {
+    griddep_wait();   // launched as a dependent of the chunk-state kernel
     __shared__ float sh[64];
     const long long row = blockIdx.y;
     const int nch = gridDim.x;
@@ -257,13 +258,17 @@ cudaError_t launch_softmax_rows(const float *x, float *z, long long rows, long l
     const bool vec4 = (T & 3) == 0 && aligned16(x) && aligned16(z);
     dim3 grid(nch, (unsigned)rows);
     float2 *w2 = reinterpret_cast<float2 *>(ws);
+    cudaError_t e;
     if (vec4) {
         softmax_chunk_state_kernel<true><<<grid, kChunkThreads, 0, s>>>(x, T, chunk, w2);
-        softmax_chunk_norm_kernel<true><<<grid, kChunkThreads, 0, s>>>(x, z, T, chunk, w2);
+        e = launch_dependent(softmax_chunk_norm_kernel<true>, grid, dim3(kChunkThreads), 0, s, x, z, T, chunk,
+                             (const float2 *)w2);
     } else {
         softmax_chunk_state_kernel<false><<<grid, kChunkThreads, 0, s>>>(x, T, chunk, w2);
-        softmax_chunk_norm_kernel<false><<<grid, kChunkThreads, 0, s>>>(x, z, T, chunk, w2);
+        e = launch_dependent(softmax_chunk_norm_kernel<false>, grid, dim3(kChunkThreads), 0, s, x, z, T, chunk,
+                             (const float2 *)w2);
     }
+    if (e != cudaSuccess) return e;
     count_launches(2);
     return cudaGetLastError();
 }

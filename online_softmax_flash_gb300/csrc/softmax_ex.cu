@@ -289,6 +289,7 @@ template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kExChunkThreads)
 softmax_ex_chunk_norm_kernel(const Tin *x, Tout *z, long long T, long long xs, long long zs, float mult,
                              long long period, long long chunk, const float2 *__restrict__ ws) {
+    griddep_wait();   // launched as a dependent of the chunk-state kernel
     __shared__ float sh[64];
     const long long row = blockIdx.y;
     const int nch = gridDim.x;
@@ -366,8 +367,9 @@ cudaError_t launch_typed(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
     dim3 grid(nch, rows);
     float2 *w2 = reinterpret_cast<float2 *>(ws);
     softmax_ex_chunk_state_kernel<Tin><<<grid, kExChunkThreads, 0, s>>>(x, q.T, q.xs, q.mult, q.period, chunk, w2);
-    softmax_ex_chunk_norm_kernel<Tin, Tout><<<grid, kExChunkThreads, 0, s>>>(x, z, q.T, q.xs, q.zs, q.mult, q.period,
-                                                                             chunk, w2);
+    cudaError_t e = launch_dependent(softmax_ex_chunk_norm_kernel<Tin, Tout>, grid, dim3(kExChunkThreads), 0, s, x, z,
+                                     q.T, q.xs, q.zs, q.mult, q.period, chunk, (const float2 *)w2);
+    if (e != cudaSuccess) return e;
     count_launches(2);
     return cudaGetLastError();
 }
