@@ -75,12 +75,18 @@ struct TcCfg {
     // K and V tiles share one ring, filled in the order they are consumed (K0 V0 K1 V1 ..., in
     // x3 mode K0h K0m K0l V0h V0l ...); the ring takes what the Q tiles leave of shared memory
     // (5 stages at D = 128, 8 in x3 mode).
-    static constexpr int FIT = (int)((kSmemLimit - 2048 - QT * TILE) / TILE);
+    // bf16 with D = 64: P goes to the MMA through shared memory (a K-major [128 x 128] tile per Q
+    // tile), so PV reads both operands from shared memory rather than P from TMEM
+    static constexpr bool PSMEM = !X3 && D == 64;
+    static constexpr uint32_t P_TILE = BM * BN * 2;
+    static constexpr uint32_t P_BYTES = PSMEM ? 2 * P_TILE : 0;
+    static constexpr int FIT = (int)((kSmemLimit - 2048 - QT * TILE - P_BYTES) / TILE);
     static constexpr int STAGES = FIT < kMaxStages ? FIT : kMaxStages;
     static_assert(!X3 || (D == 64 && STAGES >= 2 * NPOS - 2 && TILE == DBLK), "x3 mode is built for D = 64");
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t RING_OFF = QT * TILE;
-    static constexpr uint32_t SMEM_BYTES = RING_OFF + STAGES * TILE + 1024;  // + alignment slack
+    static constexpr uint32_t P_OFF = RING_OFF + STAGES * TILE;
+    static constexpr uint32_t SMEM_BYTES = P_OFF + P_BYTES + 1024;  // + alignment slack
     static constexpr int DO = X3 ? 2 * D : D;                    // TMEM columns of one O accumulator
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + DO;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);
@@ -329,7 +335,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const uint32_t dst = tmem + (t ? C::O_COL1 : C::O_COL0);
             const uint32_t pa = tmem + (t ? C::S_COL1 : C::S_COL0);
             const uint64_t vd = sdesc_sw128(sRing + sv * C::TILE, C::DBLK, 1024);
-            if constexpr (!X3) {
+            if constexpr (C::PSMEM) {
+                (void)pa;
+                const uint64_t pd = sdesc_sw128(sbase + C::P_OFF + t * C::P_TILE, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint32_t offa = ((k >> 2) * C::DBLK + (k & 3) * 32) >> 4;
+                    mma_ss(dst, pd + offa, vd + ((k * 2048) >> 4), C::IDESC_PV, acc || k > 0);
+                }
+            } else if constexpr (!X3) {
                 pv(dst, pa, vd, C::IDESC_PV, acc);
             } else {
                 const int sl = next_stage(sv);
@@ -428,6 +442,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t s_addr = lane_base + (t ? C::S_COL1 : C::S_COL0);
         const uint32_t o_addr = lane_base + (t ? C::O_COL1 : C::O_COL0);
+        const uint32_t p_smem = sbase + C::P_OFF + t * C::P_TILE;   // PSMEM: this tile's P
+        (void)p_smem;
         const float sl2 = p.scale_log2;
         const long long rows_total = (long long)p.B * p.Hq * p.Sq;
         bool ok = true;
@@ -552,9 +568,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                             acc[c] = f2_add(acc[c], f2_pack(p0, p1));
                             sr[c][k] = pack_bf16x2(p0, p1);
                         }
-                        tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5], sr[c][6],
-                                  sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13], sr[c][14],
-                                  sr[c][15]);
+                        if constexpr (C::PSMEM) {
+                            // keys 32c..32c+31 of row r: four 16-byte chunks of the 128-byte row in
+                            // block c / 2, at chunk index (c % 2) * 4 + i, XOR-swizzled by r % 8
+                            const uint32_t rowb = p_smem + (c >> 1) * C::DBLK + r * 128;
+#pragma unroll
+                            for (int i2 = 0; i2 < 4; ++i2) {
+                                const uint32_t q = (uint32_t)((c & 1) * 4 + i2);
+                                st_shared_v4(rowb + ((q ^ (uint32_t)(r & 7)) << 4), sr[c][4 * i2], sr[c][4 * i2 + 1],
+                                             sr[c][4 * i2 + 2], sr[c][4 * i2 + 3]);
+                            }
+                        } else {
+                            tmem_st16(s_addr + c * 16, sr[c][0], sr[c][1], sr[c][2], sr[c][3], sr[c][4], sr[c][5],
+                                      sr[c][6], sr[c][7], sr[c][8], sr[c][9], sr[c][10], sr[c][11], sr[c][12], sr[c][13],
+                                      sr[c][14], sr[c][15]);
+                        }
                     }
                     const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
                     float lo, hi;
@@ -582,8 +610,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     }
                 }
                 l += rs;
-                // this warp's 32 rows of P (and any rescaled O) are in TMEM
+                // this warp's 32 rows of P (and any rescaled O) are in TMEM (P: shared memory, made
+                // visible to the tensor core's async proxy)
                 tmem_st_wait();
+                if constexpr (C::PSMEM) fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[t]));
