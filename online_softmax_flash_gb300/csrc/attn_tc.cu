@@ -13,13 +13,15 @@
 //   warps 0, 2  TMA: the Q tiles once, then K (warp 0) and V (warp 2) tiles through one
 //               shared ring, one instruction per tile
 //   warp 1      MMA issue (one thread): S_t = Q_t K^T (both operands in shared memory),
-//               O_t += P_t V (P read from TMEM)
+//               O_t += P_t V (P read from TMEM; bf16 with D = 64: from shared memory)
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread r owns TMEM lane r, i.e.
 //               query row r of its tile, so row max and row sum need no cross-thread traffic.
 //
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).  P_t (bf16,
-// two per column) overwrites the first 64 columns of S_t and is read from there by the PV MMA.
-// The two Q tiles are ping-ponged so one tile's softmax overlaps the other tile's MMAs.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+DO), O_1 [256+DO,256+2DO), DO = D
+// (float32 mode: 2D).  P_t (bf16, two per column) overwrites the first 64 columns of S_t and is
+// read from there by the PV MMA; bf16 with D = 64 writes P_t to a shared-memory operand tile
+// instead; float32 mode keeps P's two parts in each 32-column chunk of S_t.  The two Q tiles are
+// ping-ponged so one tile's softmax overlaps the other tile's MMAs.
 //
 // Scores are kept in base 2 (scale * log2 e folded into one multiplier).  The rescale of O is
 // lazy: a row keeps its reference maximum until a tile raises the maximum by more than 8
@@ -43,10 +45,10 @@ constexpr int BN = 128;             // keys per key tile
 constexpr int NTHREADS = 384;       // 12 warps: 0-3 control, 4-7 softmax tile 0, 8-11 tile 1
 constexpr uint32_t TMEM_COLS = 512;
 // Register split after set-up: the two softmax warpgroups hold a whole 128-column score row
-// each; the control warpgroup (TMA + MMA issue) keeps 104.  Issuing one tcgen05.mma costs the
+// each; the control warpgroup (TMA + MMA issue) keeps 88.  Issuing one tcgen05.mma costs the
 // issuing thread about 46 cycles against 64 cycles of tensor work, so any spill or recomputation
 // in the issue loop starves the tensor pipe (its queue holds only a few instructions); below
-// about 88 registers that happened.  128*104 + 256*200 = 384*168, the registers the CTA is
+// about 88 registers that happened.  128*88 + 256*208 = 384*168, the registers the CTA is
 // launched with (168 per thread).
 constexpr int kCtrlRegs = 88, kSoftmaxRegs = 208;
 // x3 mode: the issuer carries six score products per tile and the softmax holds one chunk at a
