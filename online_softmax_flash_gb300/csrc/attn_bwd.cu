@@ -18,6 +18,7 @@
 // {64, 128} and aligned pointers normally takes the tcgen05 kernels of attn_bwd_tc.cu instead;
 // the warp-level kernels remain for pointers TMA cannot address.
 #include <mutex>
+#include <type_traits>
 
 #include "attn_bwd.cuh"
 #include "attn_bwd_tc.cuh"
@@ -48,6 +49,40 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(BwdProblem p) {
     for (int d = lane; d < p.D; d += 32) acc += ldf(o + d) * ldf(g + d);
     acc = warp_sum(acc);
     if (lane == 0) p.dvec[row] = acc;
+}
+
+// bf16 with D = 32 * VW (VW = 2 or 4 elements per lane) and rows starting on VW * 2-byte
+// boundaries: one warp per four rows, every load of the four rows issued before any arithmetic.
+template <int VW>
+__global__ void __launch_bounds__(256) bwd_rowdot_vec_kernel(BwdProblem p) {
+    using V = typename std::conditional<VW == 4, uint2, uint32_t>::type;
+    constexpr int R = 4;
+    const long long rows = (long long)p.B * p.Hq * p.Sq;
+    const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R;
+    const int lane = threadIdx.x & 31;
+    V o[R], g[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const long long row = row0 + r;
+        if (row < rows) {
+            o[r] = reinterpret_cast<const V *>(static_cast<const __nv_bfloat16 *>(p.o) + row * p.D)[lane];
+            g[r] = reinterpret_cast<const V *>(static_cast<const __nv_bfloat16 *>(p.dout) + row * p.D)[lane];
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float acc = 0.f;
+        if (row0 + r < rows) {
+            const uint32_t *ow = reinterpret_cast<const uint32_t *>(&o[r]);
+            const uint32_t *gw = reinterpret_cast<const uint32_t *>(&g[r]);
+#pragma unroll
+            for (int w = 0; w < VW / 2; ++w)
+                acc += __uint_as_float(ow[w] << 16) * __uint_as_float(gw[w] << 16) +
+                       __uint_as_float(ow[w] & 0xffff0000u) * __uint_as_float(gw[w] & 0xffff0000u);
+        }
+        acc = warp_sum(acc);
+        if (lane == r && row0 + r < rows) p.dvec[row0 + r] = acc;
+    }
 }
 
 // ------------------------------------------------------------------ CUDA-core version
@@ -492,10 +527,17 @@ bool attn_bwd_mma_supported(const BwdProblem &p) {
 cudaError_t launch_attn_bwd(const BwdProblem &p, cudaStream_t s) {
     const long long rows = (long long)p.B * p.Hq * p.Sq;
     const unsigned g = (unsigned)((rows + 7) / 8);
-    if (p.dtype == OSF_BF16)
+    const bool vec_ok = p.dtype == OSF_BF16 && (p.D == 64 || p.D == 128) &&
+                        ((reinterpret_cast<uintptr_t>(p.o) | reinterpret_cast<uintptr_t>(p.dout)) & 7u) == 0;
+    if (vec_ok) {
+        const unsigned g4 = (unsigned)((rows + 31) / 32);   // 8 warps x 4 rows per CTA
+        if (p.D == 128) bwd_rowdot_vec_kernel<4><<<g4, 256, 0, s>>>(p);
+        else bwd_rowdot_vec_kernel<2><<<g4, 256, 0, s>>>(p);
+    } else if (p.dtype == OSF_BF16) {
         bwd_rowdot_kernel<__nv_bfloat16><<<g, 256, 0, s>>>(p);
-    else
+    } else {
         bwd_rowdot_kernel<float><<<g, 256, 0, s>>>(p);
+    }
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

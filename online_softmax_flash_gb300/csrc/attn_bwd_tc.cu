@@ -447,6 +447,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         mbar_wait(dr, 0, nullptr, 20000000ull);
     } else if (warp == 2 && n > 0) {
         // ------------------------------------------------------------ per-query lse (base 2), D
+        // the kernel is a programmatic dependent of the row-sum kernel that writes D
+        griddep_wait();
         bool ok = true;
         for (int m = 0; m < n; ++m) {
             const int st = m % TSTAGES;
@@ -593,7 +595,9 @@ cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const unsigned nkv = (unsigned)((p.Sk + TB - 1) / TB) * (unsigned)(p.B * p.Hkv);
     const unsigned nq = (unsigned)((p.Sq + TB - 1) / TB) * (unsigned)(p.B * p.Hq);
-    bwd_dkdv_tc_kernel<D><<<nkv, NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
+    cudaError_t e = launch_dependent(bwd_dkdv_tc_kernel<D>, dim3(nkv), dim3(NT_THREADS), C::SMEM_BYTES, s, mq, mg, mk,
+                                     mv, p);
+    if (e != cudaSuccess) return e;
     bwd_dq_tc_kernel<D><<<nq, NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
     count_launches(2);
     return cudaGetLastError();
