@@ -27,8 +27,11 @@ def run(osf, B, Hq, Hkv, Sq, Sk, qscale, kscale, mask, seed, layout="bhsd"):
     else:
         Q, K, V = (f32_tensor(a) for a in (q, k, v))
     lse = torch.empty(B, Hq, Sq, device="cuda")
+    out = None
+    if layout == "bshd":   # the output as a [B, S, H, D] buffer seen as [B, H, S, D]
+        out = torch.full((B, Sq, Hq, D), float("nan"), device="cuda").transpose(1, 2)
     n0 = osf.osf_launch_count()
-    o = osf.osf_attn_fwd_gqa_ex(Q, K, V, mask=mask, lse=lse)
+    o = osf.osf_attn_fwd_gqa_ex(Q, K, V, out=out, mask=mask, lse=lse)
     torch.cuda.synchronize()
     launches = osf.osf_launch_count() - n0
     ref, ref_lse = oracle.attention_gqa(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), mask=mask)
@@ -57,8 +60,10 @@ def test_large_scores(osf, qscale, kscale):
 
 
 def test_key_splits_ragged_and_bshd(osf):
-    """One head, few query tiles: the key range is split and merged; ragged lengths; BSHD views."""
+    """One head, few query tiles: the key range is split and merged; ragged lengths; BSHD views
+    of the inputs and of the output."""
     run(osf, 1, 1, 1, 1000, 1537, 4.0, 2.0, "none", seed=3, layout="bshd")
+    run(osf, 2, 4, 2, 333, 333, 2.0, 2.0, "top_left", seed=5, layout="bshd")
 
 
 def test_bottom_right_rows_without_keys(osf):
