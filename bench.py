@@ -88,18 +88,20 @@ SM_COUNT_GB300 = 152
 # each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
 # source that changed since the capture reports null.
 TRAFFIC = {
-    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "8cecfe07413d0178",
-                           "bytes": 136.76e6, "scope": "attn_tc_kernel<128>, one launch"},
+    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
+                           "bytes": 136.68e6, "scope": "attn_tc_kernel<128>, one launch"},
     "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "0be7a5998426353c",
                    "bytes": 1079.08e6, "scope": "decode_kernel<128>, one launch"},
     "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ad18c62885ac3989",
                      "bytes": 1019.59e6, "scope": "softmax_rows_onchip_kernel<8>, one launch"},
     "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ad18c62885ac3989",
                    "bytes": 757.05e6, "scope": "step: chunk state + chunk normalise kernels"},
-    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "7a17f9871622aed6",
-                            "bytes": 319.17e6, "scope": "bwd_dkdv_tc_kernel<128>, one launch"},
-    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "8cecfe07413d0178",
+    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "3d79c106b0453953",
+                            "bytes": 317.77e6, "scope": "bwd_dkdv_tc_kernel<128>, one launch"},
+    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
                              "bytes": 4.33e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
+    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
+                              "bytes": 1.63e6, "scope": "attn_tc_kernel<64>, one launch (8 key splits)"},
 }
 
 
