@@ -96,8 +96,8 @@ TRAFFIC = {
                      "bytes": 1019.59e6, "scope": "softmax_rows_onchip_kernel<8>, one launch"},
     "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ad18c62885ac3989",
                    "bytes": 757.05e6, "scope": "step: chunk state + chunk normalise kernels"},
-    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "3d79c106b0453953",
-                            "bytes": 317.77e6, "scope": "bwd_dkdv_tc_kernel<128>, one launch"},
+    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "c0c998b1ef1451bf",
+                            "bytes": 521.27e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
     "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
                              "bytes": 4.33e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
     "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",

@@ -152,10 +152,11 @@ __device__ __forceinline__ void init_bars(BtBars &bars, volatile int &abort_flag
 }
 
 // ====================================================================== dQ
+// The two bodies below run as one grid (bwd_tc_kernel): CTA `bid` of each.  The tensor maps are
+// the kernel's __grid_constant__ parameters, passed by reference so TMA sees their addresses.
 template <int D>
-__global__ void __launch_bounds__(NT_THREADS, 1)
-bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mg,
-                 const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const BwdProblem p) {
+__device__ __forceinline__ void bwd_dq_body(const CUtensorMap &mq, const CUtensorMap &mg, const CUtensorMap &mk,
+                                            const CUtensorMap &mv, const BwdProblem &p, unsigned bid) {
     using C = BtCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BtBars bars;
@@ -166,8 +167,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const uint32_t sQ = sbase + C::A_OFF, sG = sQ + C::TILE, sRing = sbase + C::RING_OFF;
     // the query tiles that see the most key tiles (the last ones, under a causal mask) go first
     const int BH = p.B * p.Hq, nqt = (p.Sq + TB - 1) / TB;
-    const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * TB;
-    const int bh = blockIdx.x % BH, b = bh / p.Hq, hq = bh % p.Hq;
+    const int q0 = (nqt - 1 - (int)(bid / BH)) * TB;
+    const int bh = (int)(bid % BH), b = bh / p.Hq, hq = bh % p.Hq;
     const int kvh = hq / (p.Hq / p.Hkv);
     int n = (p.Sk + TB - 1) / TB;   // key tiles these rows see
     if (p.causal) {
@@ -263,6 +264,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         mbar_wait(dr, 0, nullptr, 20000000ull);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ compute: dS, then dQ out
+        griddep_wait();   // the grid is a programmatic dependent of the row-sum kernel (D_i)
         const int q4 = warp & 3, h = (warp - 4) >> 2;
         const int r = q4 * 32 + lane, row = q0 + r;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -347,9 +349,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 
 // ====================================================================== dK, dV
 template <int D>
-__global__ void __launch_bounds__(NT_THREADS, 1)
-bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mg,
-                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const BwdProblem p) {
+__device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUtensorMap &mg, const CUtensorMap &mk,
+                                              const CUtensorMap &mv, const BwdProblem &p, unsigned bid) {
     using C = BtCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BtBars bars;
@@ -361,8 +362,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     float *tab = reinterpret_cast<float *>(smem_raw + (sbase - smem_u32(smem_raw)) + C::TAB_OFF);
     // the key tiles seen by the most query tiles (the first ones, under a causal mask) go first
     const int BK = p.B * p.Hkv;
-    const int key0 = (int)(blockIdx.x / BK) * TB;
-    const int bk = blockIdx.x % BK, b = bk / p.Hkv, kvh = bk % p.Hkv;
+    const int key0 = (int)(bid / BK) * TB;
+    const int bk = (int)(bid % BK), b = bk / p.Hkv, kvh = bk % p.Hkv;
     const int G = p.Hq / p.Hkv;
     // query tiles that see a key of this block: from the first row that sees key0
     int q_first = p.causal ? max(0, key0 - p.causal_off) : 0;
@@ -573,17 +574,25 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     }
 }
 
+// One grid: CTAs [0, n_dkdv) are dK/dV CTAs, the rest dQ CTAs, each group heaviest first, so
+// dQ work fills the SMs the dK/dV tail leaves idle.
+template <int D>
+__global__ void __launch_bounds__(NT_THREADS, 1)
+bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mg,
+              const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const BwdProblem p,
+              unsigned n_dkdv) {
+    if (blockIdx.x < n_dkdv) bwd_dkdv_body<D>(mq, mg, mk, mv, p, blockIdx.x);
+    else bwd_dq_body<D>(mq, mg, mk, mv, p, blockIdx.x - n_dkdv);
+}
+
 template <int D>
 cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
     using C = BtCfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)C::SMEM_BYTES);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const long long qs = (long long)p.Sq * D, ks = (long long)p.Sk * D;
@@ -595,11 +604,11 @@ cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const unsigned nkv = (unsigned)((p.Sk + TB - 1) / TB) * (unsigned)(p.B * p.Hkv);
     const unsigned nq = (unsigned)((p.Sq + TB - 1) / TB) * (unsigned)(p.B * p.Hq);
-    cudaError_t e = launch_dependent(bwd_dkdv_tc_kernel<D>, dim3(nkv), dim3(NT_THREADS), C::SMEM_BYTES, s, mq, mg, mk,
-                                     mv, p);
+    if ((unsigned long long)nkv + nq >= (1ull << 31)) return cudaErrorInvalidValue;
+    cudaError_t e = launch_dependent(bwd_tc_kernel<D>, dim3(nkv + nq), dim3(NT_THREADS), C::SMEM_BYTES, s, mq, mg, mk,
+                                     mv, p, nkv);
     if (e != cudaSuccess) return e;
-    bwd_dq_tc_kernel<D><<<nq, NT_THREADS, C::SMEM_BYTES, s>>>(mq, mg, mk, mv, p);
-    count_launches(2);
+    count_launches(1);
     return cudaGetLastError();
 }
 

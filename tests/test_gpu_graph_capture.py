@@ -1,6 +1,7 @@
 """The multi-kernel calls inside a captured CUDA graph: the float32 path (split pre-pass, forward,
-combine), decode with its split combine, and the chunked 1-D softmax launch their later kernels as
-programmatic dependents of the earlier ones.  A captured call must give exactly what the same call
+combine), decode with its split combine, the chunked 1-D softmax and the tensor-core backward
+(row-sum pre-pass, then the gradient grid) launch their later kernels as programmatic dependents of
+the earlier ones.  A captured call must give exactly what the same call
 gives eagerly (every kernel here is deterministic), after the outputs have been poisoned."""
 import numpy as np
 import pytest
@@ -40,7 +41,7 @@ def test_float32_tensor_core_path_in_a_graph(osf):
     ws = torch.empty(osf.osf_attn_workspace_bytes(osf.OSF_F32, B, H, H, S, S, D), dtype=torch.uint8, device="cuda")
     n0 = osf.osf_launch_count()
     eager, got = eager_then_graph(lambda: osf.osf_attn_fwd_gqa(q, k, v, out=out, lse=lse, workspace=ws), [out, lse])
-    assert osf.osf_launch_count() - n0 >= 3   # pre-pass, forward, combine (eager run)
+    assert osf.osf_launch_count() - n0 >= 3   # pre-pass, forward, combine (counted again by the capture)
     for e, g_ in zip(eager, got):
         assert torch.equal(e, g_)
 
@@ -61,3 +62,23 @@ def test_chunked_softmax_in_a_graph(osf):
     ws = torch.empty(osf.osf_softmax_workspace_bytes(1, 1 << 22), dtype=torch.uint8, device="cuda")
     eager, got = eager_then_graph(lambda: osf.osf_softmax_rows(x, z, workspace=ws), [z])
     assert torch.equal(eager[0], got[0])
+
+
+def test_tensor_core_backward_in_a_graph(osf):
+    """The row-sum pre-pass, then one grid of dK/dV and dQ CTAs launched as its dependent."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 640, 128
+    q, k, v = (bf16_tensor(a) for a in si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=24, dtype="bf16"))
+    g = bf16_tensor(si.qkv((B, Hq, S, D), (1, 1, 1, D), seed=25, dtype="bf16")[0])
+    lse = torch.empty(B, Hq, S, device="cuda")
+    o = osf.osf_attn_fwd_gqa_ex(q, k, v, mask="top_left", lse=lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(osf.osf_attn_bwd_workspace_bytes(osf.OSF_BF16, B, Hq, Hkv, S, S, D), dtype=torch.uint8,
+                     device="cuda")
+    n0 = osf.osf_launch_count()
+    eager, got = eager_then_graph(
+        lambda: osf.osf_attn_bwd_gqa(q, k, v, o, g, lse, dq=dq, dk=dk, dv=dv, mask="top_left", workspace=ws),
+        [dq, dk, dv])
+    # pre-pass and the gradient grid, counted on the host for the eager run and for the capture
+    assert osf.osf_launch_count() - n0 == 4
+    for e, g_ in zip(eager, got):
+        assert torch.equal(e, g_)
