@@ -29,7 +29,9 @@
 //
 // Every mbarrier wait is bounded (2 s); on expiry the CTA records OSF_ERR_TIMEOUT in the
 // device status word, drains its own MMAs, lets its copies land, frees TMEM and exits.
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "attn_tc.cuh"
 #include "sm100_ptx.cuh"
@@ -158,7 +160,11 @@ __device__ __forceinline__ bool item_at(const AttnProblem &p, int n_qb, int n_it
 // Persistent: each CTA walks its work items (item_at) with one pipeline whose state -- ring
 // position, barrier phases -- carries from item to item, so an item's Q tiles and first K/V
 // tiles load while the previous item finishes.
-template <int D, bool X3>
+//
+// MERGE (key splits, one item per CTA): the CTAs of a thread-block cluster run the splits of one
+// item and merge their results through distributed shared memory at the end, instead of writing
+// partial states for a separate combine kernel.
+template <int D, bool X3, bool MERGE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mqm,
@@ -202,6 +208,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    // MERGE: a softmax thread's final row state, kept for the cluster merge at the end
+    float fin_m = -INFINITY, fin_l = 0.f;
+    bool fin_have = false;
 
     if (warp < 4) {
       setmaxnreg_dec<X3 ? kCtrlRegsX3 : kCtrlRegs>();
@@ -690,6 +699,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                         }
                     }
                     if (p.lse && row_ok) p.lse[grow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                } else if constexpr (MERGE) {
+                    // O stays in TMEM for the merge at the end
+                    fin_m = have_o ? m_ref : -INFINITY;
+                    fin_l = have_o ? l : 0.f;
+                    fin_have = have_o;
                 } else {
                     float *A = p.part_acc + ((size_t)blockIdx.y * rows_total + grow) * D;
 #pragma unroll
@@ -736,6 +750,96 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     tc_fence_before();
     __syncwarp();
     __syncthreads();
+    if constexpr (MERGE) {
+        // ------------------------------------------------------------ split merge
+        // Every MMA and copy of this CTA has completed.  Each softmax thread stages its row of O
+        // (unnormalised fp32, 16-byte chunks XOR-swizzled by row) and its (m, l) at the start of
+        // shared memory; after a cluster barrier, CTA k of the cluster merges rows [kR, kR + R)
+        // of the item from all the cluster's stages with the log-sum-exp rule, and a second
+        // barrier keeps each stage alive until every CTA has read it.  Every thread of every CTA
+        // reaches both barriers.
+        constexpr int CH = D / 4;   // 16-byte chunks per O row
+        static_assert(2 * BM * (D * 4 + 16) + 1024 <= C::SMEM_BYTES, "merge stage does not fit");
+        const uint32_t stage = sbase, ml_stage = sbase + 2 * BM * D * 4;
+        if (warp >= 4) {
+            const int t = (warp - 4) >> 2, rl = tid - 128;   // row of the item's 256
+            const uint32_t o_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (t ? C::O_COL1 : C::O_COL0);
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + c * 32, o);   // warp-collective: every lane loads
+                tmem_ld_wait();
+                if constexpr (X3) {
+                    uint32_t ob[32];
+                    tmem_ld32(o_addr + D + c * 32, ob);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) + __uint_as_float(ob[k]));
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int ch = c * 8 + q;
+                    const uint32_t a = stage + (uint32_t)rl * (D * 4) + ((uint32_t)(ch ^ (rl & (CH - 1))) << 4);
+                    if (fin_have) st_shared_v4(a, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    else st_shared_v4(a, 0u, 0u, 0u, 0u);
+                }
+            }
+            st_shared_v4(ml_stage + (uint32_t)rl * 16, __float_as_uint(fin_m), __float_as_uint(fin_l), 0u, 0u);
+        }
+        __syncwarp();
+        cluster_sync();
+        const int ns = (int)gridDim.y;   // the cluster is the item's splits
+        const int rank = (int)cluster_ctarank();
+        const int R = (2 * BM + ns - 1) / ns;
+        Item w;
+        item_at(p, n_qb, n_items, 0, w);
+        for (int task = tid; task < R * CH; task += NTHREADS) {
+            const int rl = rank * R + task / CH, ch = task % CH;
+            const int row = w.q0 + rl;
+            if (rl >= 2 * BM || row >= p.Sq) break;   // tasks go by row
+            float ms[8], ls[8], M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                ms[k] = -INFINITY;
+                ls[k] = 0.f;
+                if (k < ns) {
+                    const uint32_t a = mapa_shared(ml_stage + (uint32_t)rl * 16, (uint32_t)k);
+                    ms[k] = ld_shared_cluster_f32(a);
+                    ls[k] = ld_shared_cluster_f32(a + 4);
+                    M = fmaxf(M, ms[k]);
+                }
+            }
+            float L = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const uint32_t off = (uint32_t)rl * (D * 4) + ((uint32_t)(ch ^ (rl & (CH - 1))) << 4);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k < ns && ms[k] != -INFINITY) {   // a split that saw keys of this row
+                    const float wk = ex2_approx(ms[k] - M);
+                    const float4 v = ld_shared_cluster_v4f(mapa_shared(stage + off, (uint32_t)k));
+                    L += wk * ls[k];
+                    acc.x += wk * v.x;
+                    acc.y += wk * v.y;
+                    acc.z += wk * v.z;
+                    acc.w += wk * v.w;
+                }
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            if constexpr (X3) {
+                float *Og = static_cast<float *>(p.o) + o_at(p, w.b, w.hq, row) + ch * 4;
+                *reinterpret_cast<float4 *>(Og) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            } else {
+                __nv_bfloat16 *Og = static_cast<__nv_bfloat16 *>(p.o) + o_at(p, w.b, w.hq, row) + ch * 4;
+                *reinterpret_cast<uint2 *>(Og) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                                            pack_bf16x2(acc.z * inv, acc.w * inv));
+            }
+            if (ch == 0 && p.lse)
+                p.lse[(long long)w.bh * p.Sq + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        }
+        __syncwarp();
+        cluster_sync();
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -810,15 +914,58 @@ __global__ void __launch_bounds__(256) split_parts_kernel(const AttnProblem p, _
     }
 }
 
-template <int D, bool X3>
-cudaError_t launch_t(const AttnProblem &p, const CUtensorMap (&m)[8], int sm_count, cudaStream_t s) {
-    using C = TcCfg<D, X3>;
+template <int D, bool X3, bool MERGE>
+cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, X3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)C::SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, X3, MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)TcCfg<D, X3>::SMEM_BYTES);
     });
+    return attr_err;
+}
+
+// Whether `clusters` clusters of `ns` CTAs of the merging kernel can all run at once (one wave;
+// otherwise the splits are merged by the combine kernel).  Cached per device and cluster size.
+template <int D, bool X3>
+bool merge_fits(int clusters, int ns) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> most;   // (device, ns) -> clusters resident at once
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = most.find({dev, ns});
+    if (it == most.end()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)clusters, (unsigned)ns);
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = TcCfg<D, X3>::SMEM_BYTES;
+        cudaLaunchAttribute a;
+        a.id = cudaLaunchAttributeClusterDimension;
+        a.val.clusterDim.x = 1;
+        a.val.clusterDim.y = (unsigned)ns;
+        a.val.clusterDim.z = 1;
+        cfg.attrs = &a;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D, X3, true>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        it = most.emplace(std::make_pair(dev, ns), n).first;
+    }
+    return it->second >= clusters;
+}
+
+// `merged`: the key splits were merged inside the kernel (no combine kernel needed).
+template <int D, bool X3>
+cudaError_t launch_t(const AttnProblem &p, const CUtensorMap (&m)[8], int sm_count, cudaStream_t s, bool &merged) {
+    using C = TcCfg<D, X3>;
+    merged = false;
+    cudaError_t attr_err = set_smem_attr<D, X3, false>();
     if (attr_err != cudaSuccess) return attr_err;
     const int n_qb = (p.Sq + 2 * BM - 1) / (2 * BM);
     const long long items = (long long)n_qb * p.B * p.Hq;
@@ -826,32 +973,41 @@ cudaError_t launch_t(const AttnProblem &p, const CUtensorMap (&m)[8], int sm_cou
     // one resident CTA per SM walks the items; fewer items than SMs: one CTA per item
     const int grid = (int)(items < sm_count ? items : (sm_count > 0 ? sm_count : 1));
     const dim3 g((unsigned)grid, (unsigned)p.splits);
-    if (X3) {
+    // key splits of few items: a cluster per item when its splits fit one (portable size 8)
+    // and all clusters run at once
+    if (p.splits > 1 && p.splits <= 8 && items < sm_count && set_smem_attr<D, X3, true>() == cudaSuccess &&
+        merge_fits<D, X3>(grid, p.splits)) {
+        cudaError_t e = launch_clustered(attn_tc_kernel<D, X3, true>, g, dim3(NTHREADS), C::SMEM_BYTES, s,
+                                         dim3(1, (unsigned)p.splits, 1), X3, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+                                         m[7], p, n_qb, (int)items);
+        if (e != cudaSuccess) return e;
+        merged = true;
+    } else if (X3) {
         // dependent of the split pre-pass (see the producers' griddep_wait)
-        cudaError_t e = launch_dependent(attn_tc_kernel<D, X3>, g, dim3(NTHREADS), C::SMEM_BYTES, s, m[0], m[1], m[2],
-                                         m[3], m[4], m[5], m[6], m[7], p, n_qb, (int)items);
+        cudaError_t e = launch_dependent(attn_tc_kernel<D, X3, false>, g, dim3(NTHREADS), C::SMEM_BYTES, s, m[0],
+                                         m[1], m[2], m[3], m[4], m[5], m[6], m[7], p, n_qb, (int)items);
         if (e != cudaSuccess) return e;
     } else {
-        attn_tc_kernel<D, X3><<<g, NTHREADS, C::SMEM_BYTES, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p,
-                                                                  n_qb, (int)items);
+        attn_tc_kernel<D, X3, false><<<g, NTHREADS, C::SMEM_BYTES, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
+                                                                         p, n_qb, (int)items);
     }
     count_launches(1);
     return cudaGetLastError();
 }
 
 // bf16 inputs: maps on the caller's tensors (the part maps are unused copies).
-cudaError_t launch_bf16(const AttnProblem &p, int sm_count, cudaStream_t s) {
+cudaError_t launch_bf16(const AttnProblem &p, int sm_count, cudaStream_t s, bool &merged) {
     CUtensorMap m[8];
     if (!make_maps(p, &m[0], &m[1], &m[2])) return cudaErrorInvalidValue;
     m[3] = m[6] = m[0];
     m[4] = m[7] = m[1];
     m[5] = m[2];
-    return p.D == 64 ? launch_t<64, false>(p, m, sm_count, s) : launch_t<128, false>(p, m, sm_count, s);
+    return p.D == 64 ? launch_t<64, false>(p, m, sm_count, s, merged) : launch_t<128, false>(p, m, sm_count, s, merged);
 }
 
 // float32 inputs (D = 64): split Q, K, V into bf16 parts in the workspace, then run x3 mode on
 // contiguous maps of the parts.  Map order: Qh Kh Vh Qm Km Ql Kl Vl.
-cudaError_t launch_x3(const AttnProblem &p, int sm_count, cudaStream_t s) {
+cudaError_t launch_x3(const AttnProblem &p, int sm_count, cudaStream_t s, bool &merged) {
     const long long nq = (long long)p.B * p.Hq * p.Sq * p.D, nk = (long long)p.B * p.Hkv * p.Sk * p.D;
     __nv_bfloat16 *ws = static_cast<__nv_bfloat16 *>(p.x3_ws);
     if (!ws) return cudaErrorInvalidValue;
@@ -877,13 +1033,15 @@ cudaError_t launch_x3(const AttnProblem &p, int sm_count, cudaStream_t s) {
     if (!qmap(&m[0], q[0]) || !kmap(&m[1], k[0]) || !kmap(&m[2], v[0]) || !qmap(&m[3], q[1]) ||
         !kmap(&m[4], k[1]) || !qmap(&m[5], q[2]) || !kmap(&m[6], k[2]) || !kmap(&m[7], v[1]))
         return cudaErrorInvalidValue;
-    return launch_t<64, true>(p, m, sm_count, s);
+    return launch_t<64, true>(p, m, sm_count, s, merged);
 }
 
 // CTAs the kernel runs for a problem (before any key split).
 long long tc_ctas(const AttnProblem &p) {
     return (long long)((p.Sq + 2 * BM - 1) / (2 * BM)) * p.B * p.Hq;
 }
+
+
 
 }  // namespace
 
@@ -915,15 +1073,19 @@ int attn_tc_pick_splits(const AttnProblem &p, int sm_count) {
     const long long ctas = tc_ctas(p);
     const int n_kt = (p.Sk + BN - 1) / BN;
     if (ctas >= sm_count || n_kt <= 1) return 1;
-    int want = (int)((sm_count + ctas - 1) / ctas);
+    // as many splits as keep every CTA in one wave (one CTA per SM): a second wave would cost
+    // more than the extra split saves
+    int want = (int)(sm_count / ctas);
     if (want > n_kt) want = n_kt;
+    if (want < 2) return 1;
     const int tps = (n_kt + want - 1) / want;
     return (n_kt + tps - 1) / tps;   // no empty split
 }
 
 cudaError_t launch_attn_tc(const AttnProblem &p, int sm_count, cudaStream_t s) {
-    cudaError_t e = p.dtype == OSF_F32 ? launch_x3(p, sm_count, s) : launch_bf16(p, sm_count, s);
-    if (e == cudaSuccess && p.splits > 1) e = launch_attn_combine(p, s);
+    bool merged = false;
+    cudaError_t e = p.dtype == OSF_F32 ? launch_x3(p, sm_count, s, merged) : launch_bf16(p, sm_count, s, merged);
+    if (e == cudaSuccess && p.splits > 1 && !merged) e = launch_attn_combine(p, s);
     return e;
 }
 
