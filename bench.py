@@ -88,8 +88,8 @@ SM_COUNT_GB300 = 152
 # each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
 # source that changed since the capture reports null.
 TRAFFIC = {
-    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
-                           "bytes": 136.68e6, "scope": "attn_tc_kernel<128>, one launch"},
+    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
+                           "bytes": 136.32e6, "scope": "attn_tc_kernel<128>, one launch"},
     "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "0be7a5998426353c",
                    "bytes": 1079.08e6, "scope": "decode_kernel<128>, one launch"},
     "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ad18c62885ac3989",
@@ -98,9 +98,9 @@ TRAFFIC = {
                    "bytes": 757.05e6, "scope": "step: chunk state + chunk normalise kernels"},
     "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "c0c998b1ef1451bf",
                             "bytes": 521.27e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
-    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
+    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
                              "bytes": 4.33e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
-    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "28564406a85e1b1d",
+    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
                               "bytes": 1.63e6, "scope": "attn_tc_kernel<64>, one launch (8 key splits)"},
 }
 
