@@ -110,6 +110,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// Ask the bulk-copy engine to bring `bytes` of global memory at `src` into L2 (no completion
+// signal; both 16-byte aligned multiples).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // Load through a 5-D map at coordinates (c0..c4), completing on `bar`.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1, int c2,
                                             int c3, int c4) {

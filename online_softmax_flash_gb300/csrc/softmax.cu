@@ -11,7 +11,10 @@
 //    holds the whole row in registers (up to 8 float4 per thread).  Each thread reduces its
 //    values to a local (m, l); the CTA merges the states with the recurrence, and the outputs
 //    are produced from the registers: one HBM read and one HBM write per element, instead of
-//    the two reads of the pages' single-program loop (the row fits on chip).
+//    the two reads of the pages' single-program loop (the row fits on chip).  Where such a CTA
+//    is alone on its SM (by its register use, rows of more than about 13000 elements),
+//    persistent CTAs walk the rows and prefetch each next row into L2 while they reduce and
+//    write the current one.
 //  * chunked rows (longer rows, e.g. the 1-D vector, or unaligned data): kernel 1 splits each
 //    row into chunks, one CTA per chunk, and writes each chunk's (m, l); kernel 2 merges a
 //    row's chunk states and normalises its chunk -- the pages' two passes (two reads, one
@@ -19,7 +22,13 @@
 //    backwards so the part kernel 1 read last is still in L2.
 //
 // All exponentials are base 2 on x * log2(e).
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "osf_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace osf {
 namespace {
@@ -94,6 +103,57 @@ softmax_rows_onchip_kernel(const float *__restrict__ x, float *z, int T) {
             float4 o = v[k];
             o.x *= f; o.y *= f; o.z *= f; o.w *= f;
             __stcs(zr + i, o);
+        }
+    }
+}
+
+// Persistent form of the on-chip kernel: CTA b takes rows b, b + gridDim.x, ...; before it
+// reduces a row it asks the bulk-copy engine to prefetch its next row into L2, so the HBM read
+// of that row runs while this one is reduced and written (a CTA holding a whole row in
+// registers is otherwise alone on its SM and leaves HBM idle between its read and its writes).
+template <int VPT>
+__global__ void __launch_bounds__(1024, 1)
+softmax_rows_resident_kernel(const float *__restrict__ x, float *z, long long rows, int T) {
+    __shared__ float sh[2][64];
+    const int nvec = T >> 2;
+    const uint32_t row_bytes = (uint32_t)T * 4u;
+    int par = 0;
+    for (long long row = blockIdx.x; row < rows; row += gridDim.x, par ^= 1) {
+        const float4 *xr = reinterpret_cast<const float4 *>(x + row * (long long)T);
+        float4 *zr = reinterpret_cast<float4 *>(z + row * (long long)T);
+        if (threadIdx.x == 0 && row + gridDim.x < rows)
+            ptx::prefetch_l2_bulk(x + (row + gridDim.x) * (long long)T, row_bytes);
+        float4 v[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int i = threadIdx.x + k * blockDim.x;
+            v[k] = i < nvec ? __ldcs(xr + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            v[k].x *= kLog2e; v[k].y *= kLog2e; v[k].z *= kLog2e; v[k].w *= kLog2e;
+            m = fmaxf(m, fmaxf(fmaxf(v[k].x, v[k].y), fmaxf(v[k].z, v[k].w)));
+        }
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        float l = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            v[k].x = ex2_approx(v[k].x - mref); v[k].y = ex2_approx(v[k].y - mref);
+            v[k].z = ex2_approx(v[k].z - mref); v[k].w = ex2_approx(v[k].w - mref);
+            l += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+        }
+        float M = m, L = l;
+        block_merge_ml(M, L, sh[par]);   // alternate halves: no barrier needed between rows
+        const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - M) / L;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int i = threadIdx.x + k * blockDim.x;
+            if (i < nvec) {
+                float4 o = v[k];
+                o.x *= f; o.y *= f; o.z *= f; o.w *= f;
+                __stcs(zr + i, o);
+            }
         }
     }
 }
@@ -229,6 +289,37 @@ size_t softmax_workspace_floats(long long rows, long long T, int sm_count) {
     return (size_t)rows * nch * 2;
 }
 
+// Resident CTAs per SM of `kernel` at `threads` threads (no dynamic shared memory), cached
+// per device, kernel and CTA size.
+int blocks_per_sm(const void *kernel, int threads) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(dev, kernel, threads);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+    cache[key] = n;
+    return n;
+}
+
+template <int VPT>
+cudaError_t launch_rows(const float *x, float *z, long long rows, int T, int threads, int sm_count,
+                        cudaStream_t s) {
+    if (VPT >= 4 && blocks_per_sm((const void *)softmax_rows_onchip_kernel<VPT>, threads) == 1) {
+        // one CTA per row would be alone on its SM: persistent CTAs prefetching their next row
+        const int per_sm = blocks_per_sm((const void *)softmax_rows_resident_kernel<VPT>, threads);
+        const long long grid = std::min<long long>(rows, (long long)per_sm * sm_count);
+        softmax_rows_resident_kernel<VPT><<<(unsigned)grid, threads, 0, s>>>(x, z, rows, T);
+    } else {
+        softmax_rows_onchip_kernel<VPT><<<(unsigned)rows, threads, 0, s>>>(x, z, T);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_softmax_rows(const float *x, float *z, long long rows, long long T,
                                 float *ws, int sm_count, cudaStream_t s) {
     if (onchip_ok(x, z, T)) {
@@ -237,13 +328,14 @@ cudaError_t launch_softmax_rows(const float *x, float *z, long long rows, long l
         while (vpt < 8 && nvec > 1024 * vpt) vpt *= 2;
         int threads = (nvec + vpt - 1) / vpt;
         threads = ((threads + 31) / 32) * 32;
-        const unsigned grid = (unsigned)rows;
+        cudaError_t e;
         switch (vpt) {
-            case 1: softmax_rows_onchip_kernel<1><<<grid, threads, 0, s>>>(x, z, (int)T); break;
-            case 2: softmax_rows_onchip_kernel<2><<<grid, threads, 0, s>>>(x, z, (int)T); break;
-            case 4: softmax_rows_onchip_kernel<4><<<grid, threads, 0, s>>>(x, z, (int)T); break;
-            default: softmax_rows_onchip_kernel<8><<<grid, threads, 0, s>>>(x, z, (int)T); break;
+            case 1: e = launch_rows<1>(x, z, rows, (int)T, threads, sm_count, s); break;
+            case 2: e = launch_rows<2>(x, z, rows, (int)T, threads, sm_count, s); break;
+            case 4: e = launch_rows<4>(x, z, rows, (int)T, threads, sm_count, s); break;
+            default: e = launch_rows<8>(x, z, rows, (int)T, threads, sm_count, s); break;
         }
+        if (e != cudaSuccess) return e;
         count_launches(1);
         return cudaGetLastError();
     }

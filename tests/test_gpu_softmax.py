@@ -45,7 +45,7 @@ def test_softmax_1d_full_size(osf):
 
 
 @pytest.mark.parametrize("rows", [1, 3, 64])
-@pytest.mark.parametrize("T", [1, 3, 4, 100, 1000, 4096, 32767, 32768, 32772, 100003])
+@pytest.mark.parametrize("T", [1, 3, 4, 100, 1000, 4096, 8196, 20004, 32767, 32768, 32772, 100003])
 def test_softmax_shapes(osf, rows, T):
     x = si.softmax_rows_input(rows, T, seed=rows * 7 + T)
     check_rows(run(osf, x), oracle.softmax(x), f"rows={rows} T={T}")
@@ -57,8 +57,8 @@ def test_softmax_in_place(osf, T):
     check_rows(run(osf, x, inplace=True), oracle.softmax(x), f"in place T={T}")
 
 
-def test_softmax_special_rows(osf):
-    T = 4096
+@pytest.mark.parametrize("T", [4096, 16384])
+def test_softmax_special_rows(osf, T):
     x = np.zeros((5, T), dtype=np.float32)
     x[0] = 3.25                      # constant row -> uniform
     x[1] = -200.0                    # all very negative -> uniform (initial max must be -inf)
@@ -67,7 +67,7 @@ def test_softmax_special_rows(osf):
     x[3, :7] = np.arange(7)          # ... except seven
     x[4] = si.normal_f32((T,), 4, si.STREAM_X, 1e3)   # huge spread
     z = run(osf, x)
-    check_rows(z, oracle.softmax(x), "special rows")
+    check_rows(z, oracle.softmax(x), f"special rows T={T}")
     assert np.all(z[3, 7:] == 0)
 
 
