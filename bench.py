@@ -92,10 +92,10 @@ TRAFFIC = {
                            "bytes": 136.32e6, "scope": "attn_tc_kernel<128>, one launch"},
     "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "0be7a5998426353c",
                    "bytes": 1079.08e6, "scope": "decode_kernel<128>, one launch"},
-    "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ad18c62885ac3989",
-                     "bytes": 1019.59e6, "scope": "softmax_rows_onchip_kernel<8>, one launch"},
-    "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ad18c62885ac3989",
-                   "bytes": 757.05e6, "scope": "step: chunk state + chunk normalise kernels"},
+    "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
+                     "bytes": 1012.50e6, "scope": "softmax_rows_resident_kernel<8>, one launch"},
+    "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
+                   "bytes": 756.78e6, "scope": "step: chunk state + chunk normalise kernels"},
     "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "c0c998b1ef1451bf",
                             "bytes": 521.27e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
     "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
@@ -573,7 +573,14 @@ def main():
     ap.add_argument("--suite-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time (cpu_baseline)")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds per reference-arm step")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="row count of a softmax workload instead of its own (a smaller case to profile)")
     args = ap.parse_args()
+    if args.rows:
+        w0 = WORKLOADS[args.workload]
+        if w0["kind"] != "softmax" or args.rows < 1:
+            ap.error("--rows takes a positive count and applies to the softmax workloads only")
+        WORKLOADS[args.workload] = dict(w0, rows=args.rows, desc=f"{w0['desc']} (rows set to {args.rows})")
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         return reference_arm(args, world, rank)
