@@ -6,6 +6,9 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
+#include <set>
+#include <tuple>
 
 #include "osf_internal.cuh"
 #include "softmax_ex.cuh"
@@ -19,6 +22,20 @@ namespace osf {
 static std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static std::set<std::tuple<int, const void *, int>> done;   // (device, kernel, bytes)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(dev, kernel, bytes);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -29,7 +46,7 @@ __device__ int g_status_word;
 struct DeviceInfo {
     int sm_count = 0;
     int *status = nullptr;   // device address of g_status_word
-    bool ready = false;
+    std::atomic<bool> ready{false};   // set (release) after the fields above
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -38,21 +55,25 @@ int current_device(int *dev) {
     return OSF_OK;
 }
 
-// Per-device set-up (SM count, status word address).  Idempotent; concurrent first calls
-// compute the same values.
+// Per-device set-up (SM count, status word address), once per device under a lock; later
+// calls see the published fields through the acquire load of `ready`.
 int device_info(DeviceInfo **out) {
+    static std::mutex mu;
     int dev;
     if (current_device(&dev) != OSF_OK) return OSF_ERR_CUDA;
     DeviceInfo &d = g_dev[dev];
-    if (!d.ready) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return OSF_ERR_CUDA;
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return OSF_ERR_CUDA;
-        d.sm_count = sms;
-        d.status = static_cast<int *>(addr);
-        d.ready = true;
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return OSF_ERR_CUDA;
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return OSF_ERR_CUDA;
+            d.sm_count = sms;
+            d.status = static_cast<int *>(addr);
+            d.ready.store(true, std::memory_order_release);
+        }
     }
     *out = &d;
     return OSF_OK;

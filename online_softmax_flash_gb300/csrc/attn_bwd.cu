@@ -488,15 +488,8 @@ cudaError_t launch_mma(const BwdProblem &p, cudaStream_t s) {
     constexpr int LD = C::LD;
     const size_t smem_kv = (size_t)(2 * 64 + 2 * C::BQ) * LD * 2 + 2 * C::BQ * 4;
     const size_t smem_q = (size_t)(2 * 64 + 2 * C::BK) * LD * 2 + 2 * 64 * 4;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(bwd_dkdv_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem_kv);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(bwd_dq_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)smem_q);
-    });
+    cudaError_t attr_err = set_max_dynamic_smem((const void *)bwd_dkdv_mma_kernel<D>, (int)smem_kv);
+    if (attr_err == cudaSuccess) attr_err = set_max_dynamic_smem((const void *)bwd_dq_mma_kernel<D>, (int)smem_q);
     if (attr_err != cudaSuccess) return attr_err;
     bwd_dkdv_mma_kernel<D><<<dim3((p.Sk + 63) / 64, p.B * p.Hkv), 128, smem_kv, s>>>(p);
     bwd_dq_mma_kernel<D><<<dim3((p.Sq + 63) / 64, p.B * p.Hq), 128, smem_q, s>>>(p);

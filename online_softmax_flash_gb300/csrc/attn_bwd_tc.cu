@@ -588,12 +588,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 template <int D>
 cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
     using C = BtCfg<D>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)C::SMEM_BYTES);
-    });
+    const cudaError_t attr_err = set_max_dynamic_smem((const void *)bwd_tc_kernel<D>, (int)C::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
     const long long qs = (long long)p.Sq * D, ks = (long long)p.Sk * D;
     CUtensorMap mq, mg, mk, mv;

@@ -278,14 +278,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnProblem p) 
 template <typename T, int DP, int BM>
 cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     using C = SimtCfg<DP, BM>;
-    static bool configured = false;   // attribute is per function; idempotent, benign race
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, DP, BM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    const cudaError_t e = set_max_dynamic_smem((const void *)attn_simt_kernel<T, DP, BM>, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     dim3 grid((p.Sq + BM - 1) / BM, p.B * p.Hq, p.splits);
     attn_simt_kernel<T, DP, BM><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(p);
     count_launches(1);

@@ -916,13 +916,7 @@ __global__ void __launch_bounds__(256) split_parts_kernel(const AttnProblem p, _
 
 template <int D, bool X3, bool MERGE>
 cudaError_t set_smem_attr() {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, X3, MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)TcCfg<D, X3>::SMEM_BYTES);
-    });
-    return attr_err;
+    return set_max_dynamic_smem((const void *)attn_tc_kernel<D, X3, MERGE>, (int)TcCfg<D, X3>::SMEM_BYTES);
 }
 
 // Whether `clusters` clusters of `ns` CTAs of the merging kernel can all run at once (one wave;

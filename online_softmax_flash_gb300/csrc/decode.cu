@@ -272,11 +272,7 @@ bool make_maps(const AttnProblem &p, CUtensorMap *mk, CUtensorMap *mv) {
 template <int D>
 cudaError_t launch_t(const AttnProblem &p, cudaStream_t s) {
     using C = DecCfg<D>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    });
+    const cudaError_t attr_err = set_max_dynamic_smem((const void *)decode_kernel<D>, (int)C::SMEM);
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap mk, mv;
     if (!make_maps(p, &mk, &mv)) return cudaErrorInvalidValue;

@@ -92,6 +92,10 @@ __host__ __device__ __forceinline__ long long o_at(const AttnProblem &p, int b, 
 
 // Count of kernels launched by the library (diagnostics; see osf_launch_count).
 void count_launches(int n);
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device.  The attribute
+// belongs to the device's context, so every device is configured on its first use there;
+// thread-safe, and a no-op once a device is configured.
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
 // Launch `kernel` as a programmatic dependent of the previous kernel in the stream: it is
 // scheduled as soon as every block of that kernel has finished, without the launch gap, and

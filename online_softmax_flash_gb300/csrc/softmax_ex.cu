@@ -317,12 +317,8 @@ cudaError_t launch_typed(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
     const bool aligned = q.T % E == 0 && al16(x, q.xs * (long long)sizeof(Tin)) &&
                          al16(z, q.zs * (long long)sizeof(Tout));
     if (aligned && (uint64_t)q.T * sizeof(Tin) <= kSmemRowBytes) {
-        static std::once_flag once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(once, [] {
-            attr_err = cudaFuncSetAttribute(softmax_ex_smem_kernel<Tin, Tout, 256>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRowBytes);
-        });
+        const cudaError_t attr_err =
+            set_max_dynamic_smem((const void *)softmax_ex_smem_kernel<Tin, Tout, 256>, (int)kSmemRowBytes);
         if (attr_err != cudaSuccess) return attr_err;
         const size_t smem = (size_t)q.T * sizeof(Tin);
         if (smem <= 8 * 1024)
