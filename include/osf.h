@@ -162,6 +162,33 @@ int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, 
                              size_t *bytes);
 
 /*
+ * osf_attn_fwd_gqa_host -- osf_attn_fwd_gqa on HOST buffers: the attention of [Q3]
+ * "自注意力原理" + "GQA" (the same operation, mask rule and scale as osf_attn_fwd_gqa; the pages
+ * pass tensors that are already on the GPU, so this copying variant has no counterpart there).
+ * Q, K, V: host pointers to contiguous [B, Hq, Sq, D] / [B, Hkv, Sk, D] arrays of `dtype`;
+ * O: host pointer to [B, Hq, Sq, D], written.  Page-locked (pinned) host memory lets the copies
+ * run asynchronously and overlap; pageable memory works but the copies then block the host.
+ * device_buffer: caller-owned device memory of at least osf_attn_host_buffer_bytes bytes; it
+ *     receives device copies of Q, K, V, O and the kernels' scratch (too small or NULL ->
+ *     OSF_ERR_WORKSPACE).
+ * The problem is cut into up to 8 chunks of whole (batch, kv head) units, each a contiguous
+ * range of every tensor; chunk c's host-to-device copies, its attention and its device-to-host
+ * copy are enqueued on an internal copy-in stream, `stream` and an internal copy-out stream,
+ * linked by events, so copies overlap computation and each other.  All of it is ordered after
+ * the work already on `stream`, and work enqueued on `stream` afterwards runs after O has
+ * reached the host: synchronise `stream` before reading O.  The first call on a device creates
+ * the two copy streams and their events (kept until exit); calls are serialised while they
+ * enqueue.  lse is not produced.  Sizes, errors and emptiness as in osf_attn_fwd_gqa.
+ */
+int osf_attn_fwd_gqa_host(const void *Q, const void *K, const void *V, void *O, int dtype,
+                          int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                          void *device_buffer, size_t device_buffer_bytes, osf_stream stream);
+
+/* Device bytes osf_attn_fwd_gqa_host needs in device_buffer for these arguments. */
+int osf_attn_host_buffer_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                               size_t *bytes);
+
+/*
  * osf_attn_decode_gqa -- the Sq == 1 path of osf_attn_fwd_gqa with an explicit split count.
  * The Sk keys of each (b, kv head) are cut into `num_splits` contiguous chunks; each chunk
  * yields a partial state (m_s, l_s, acc_s) and a combine step merges them with the

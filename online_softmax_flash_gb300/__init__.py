@@ -19,6 +19,7 @@ __all__ = [
     "osf_softmax_rows", "osf_softmax_workspace_bytes", "osf_device_status", "osf_launch_count",
     "solve", "osf_attn_fwd_gqa_ex", "osf_softmax_rows_ex", "osf_softmax_ex_workspace_bytes",
     "osf_attn_bwd_gqa", "osf_attn_bwd_workspace_bytes", "osf_selftest_bounded_wait", "OSF_MASK_NONE", "OSF_MASK_TOP_LEFT", "OSF_MASK_BOTTOM_RIGHT",
+    "osf_attn_fwd_gqa_host", "osf_attn_host_buffer_bytes",
 ]
 
 OSF_OK, OSF_ERR_INVALID, OSF_ERR_UNSUPPORTED, OSF_ERR_CUDA, OSF_ERR_TIMEOUT, OSF_ERR_WORKSPACE = range(6)
@@ -36,6 +37,8 @@ _SIGS = {
     "osf_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "osf_attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "osf_attn_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "osf_attn_fwd_gqa_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "osf_attn_host_buffer_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "osf_attn_fwd_gqa_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "osf_attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
     "osf_attn_decode_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
@@ -159,6 +162,43 @@ def osf_attn_fwd_gqa(q, k, v, out=None, causal: bool = False, scale: float | Non
                                   int(bool(causal)), 0.0 if scale is None else float(scale),
                                   _ptr(lse), _ptr(ws), ws_bytes, _stream(q.device)),
            "osf_attn_fwd_gqa")
+    return out
+
+
+def osf_attn_host_buffer_bytes(dtype: int, B, Hq, Hkv, Sq, Sk, D, causal: bool = False) -> int:
+    n = _sz(0)
+    _check(lib().osf_attn_host_buffer_bytes(dtype, B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), ctypes.byref(n)),
+           "osf_attn_host_buffer_bytes")
+    return n.value
+
+
+def osf_attn_fwd_gqa_host(q, k, v, out=None, causal: bool = False, scale: float | None = None,
+                          device_buffer=None, device=None):
+    """osf_attn_fwd_gqa on host (CPU) tensors: the library copies them in, runs the attention and
+    copies O back, overlapping the copies with the computation; ``out`` (a host tensor, pinned if
+    ``q`` is) is allocated if None.  ``device_buffer``: a CUDA uint8 tensor of at least
+    osf_attn_host_buffer_bytes bytes, allocated on ``device`` (default: the current device) if
+    None.  Returns ``out``, which holds the result once the device's current stream has reached
+    the end of the call (synchronise it before reading)."""
+    for t in (q, k, v, out):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("osf_attn_fwd_gqa_host takes contiguous host tensors")
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    n = osf_attn_host_buffer_bytes(dt, B, Hq, Hkv, Sq, Sk, D, causal)
+    if device_buffer is None:
+        device_buffer = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    _need_cuda(device_buffer)
+    nb = device_buffer.numel() * device_buffer.element_size()
+    with torch.cuda.device(device_buffer.device):
+        _check(lib().osf_attn_fwd_gqa_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), dt, B, Hq, Hkv, Sq, Sk, D,
+                                           int(bool(causal)), 0.0 if scale is None else float(scale),
+                                           _ptr(device_buffer), nb, _stream(device_buffer.device)),
+               "osf_attn_fwd_gqa_host")
     return out
 
 

@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <set>
@@ -268,6 +269,91 @@ int run_gqa(AttnProblem &p, Path path, void *workspace, size_t workspace_bytes, 
     }
 }
 
+// ------------------------------------------------------------- host buffers in and out
+// osf_attn_fwd_gqa_host splits the problem into chunks of whole (batch, kv head) units: unit u =
+// b * Hkv + g owns the G query heads g*G .. g*G+G-1 of batch b and kv head g, so a run of
+// consecutive units is one contiguous range of Q, K, V and O, and a chunk of n units is itself a
+// GQA problem with B = n, Hq = G, Hkv = 1.  Each chunk's copies in, attention and copy out are
+// enqueued on three streams (copy-in, the caller's, copy-out) linked by events, so the copies of
+// one chunk overlap the attention of another and the two copy directions overlap each other.
+constexpr int kHostChunks = 8;
+
+struct HostUnits {
+    long long units = 0;      // B * Hkv
+    int chunks = 0;           // number of chunks
+    long long per = 0;        // units per chunk (the last may have fewer)
+    size_t q_unit = 0, kv_unit = 0;   // bytes of one unit's Q (and O) and of its K (and V)
+};
+
+HostUnits host_units(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D) {
+    HostUnits h;
+    const int G = Hq / Hkv;
+    h.units = (long long)B * Hkv;
+    h.chunks = (int)std::min<long long>(h.units, kHostChunks);
+    h.per = (h.units + h.chunks - 1) / h.chunks;
+    h.chunks = (int)((h.units + h.per - 1) / h.per);
+    h.q_unit = (size_t)G * Sq * D * elem_size(dtype);
+    h.kv_unit = (size_t)Sk * D * elem_size(dtype);
+    return h;
+}
+
+// Device-buffer layout: Q | K | V | O | chunk workspace, each piece 256-byte aligned.
+struct HostLayout {
+    size_t q = 0, k = 0, v = 0, o = 0, ws = 0, ws_bytes = 0, total = 0;
+};
+
+int host_layout(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D, HostLayout &L) {
+    const HostUnits h = host_units(dtype, B, Hq, Hkv, Sq, Sk, D);
+    const size_t qb = h.q_unit * h.units, kvb = h.kv_unit * h.units;
+    // workspace: the larger need of a full chunk and of the last (smaller) one
+    size_t ws = 0;
+    const long long sizes[2] = {h.per, h.units - (long long)(h.chunks - 1) * h.per};
+    for (long long n : sizes) {
+        size_t w = 0;
+        const int st = osf_attn_workspace_bytes(dtype, (int)n, Hq / Hkv, 1, Sq, Sk, D, &w);
+        if (st != OSF_OK) return st;
+        ws = std::max(ws, w);
+    }
+    L.q = 0;
+    L.k = align256(qb);
+    L.v = L.k + align256(kvb);
+    L.o = L.v + align256(kvb);
+    L.ws = L.o + align256(qb);
+    L.ws_bytes = ws;
+    L.total = L.ws + align256(ws);
+    return OSF_OK;
+}
+
+// Per-device copy streams and events, created on the first host-buffer call on the device.
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t landed[kHostChunks] = {}, computed[kHostChunks] = {};
+    bool ready = false;
+};
+HostStreams g_host[kMaxDevices];
+std::mutex g_host_mutex;   // held while a call enqueues its work (the events are shared)
+
+int host_streams(HostStreams **out) {
+    int dev;
+    if (current_device(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    HostStreams &h = g_host[dev];
+    if (!h.ready) {
+        if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) != cudaSuccess)
+            return OSF_ERR_CUDA;
+        for (int i = 0; i < kHostChunks; ++i)
+            if (cudaEventCreateWithFlags(&h.landed[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h.computed[i], cudaEventDisableTiming) != cudaSuccess)
+                return OSF_ERR_CUDA;
+        h.ready = true;
+    }
+    *out = &h;
+    return OSF_OK;
+}
+
 }  // namespace
 }  // namespace osf
 
@@ -364,6 +450,82 @@ int osf_attn_fwd_gqa_ex(const void *Q, const void *K, const void *V, void *O, in
     const Path path = choose_path(p, Q, K, V, O);
     const int splits = plan_splits(p, path, dev->sm_count, 0);
     return run_gqa(p, path, workspace, workspace_bytes, splits, dev, (cudaStream_t)stream);
+}
+
+int osf_attn_host_buffer_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                               size_t *bytes) {
+    if (!bytes) return OSF_ERR_INVALID;
+    *bytes = 0;
+    AttnProblem p;
+    bool empty;
+    const void *ph = reinterpret_cast<const void *>(uintptr_t(1) << 40);
+    int st = check_gqa(ph, ph, ph, reinterpret_cast<void *>(uintptr_t(1) << 44), dtype, B, Hq, Hkv,
+                       Sq, Sk, D, causal, 0.f, nullptr, p, empty);
+    if (st != OSF_OK || empty) return st;
+    HostLayout L;
+    st = host_layout(dtype, B, Hq, Hkv, Sq, Sk, D, L);
+    if (st != OSF_OK) return st;
+    *bytes = L.total;
+    return OSF_OK;
+}
+
+int osf_attn_fwd_gqa_host(const void *Q, const void *K, const void *V, void *O, int dtype, int B,
+                          int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                          void *device_buffer, size_t device_buffer_bytes, osf_stream stream) {
+    AttnProblem p;
+    bool empty;
+    // validate the sizes and the host pointers as a whole problem
+    int st = check_gqa(Q, K, V, O, dtype, B, Hq, Hkv, Sq, Sk, D, causal, scale, nullptr, p, empty);
+    if (st != OSF_OK || empty) return st;
+    if (!device_buffer) return OSF_ERR_WORKSPACE;
+    HostLayout L;
+    st = host_layout(dtype, B, Hq, Hkv, Sq, Sk, D, L);
+    if (st != OSF_OK) return st;
+    if (device_buffer_bytes < L.total) return OSF_ERR_WORKSPACE;
+    DeviceInfo *dev;
+    if (device_info(&dev) != OSF_OK) return OSF_ERR_CUDA;
+    HostStreams *hs;
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    if (host_streams(&hs) != OSF_OK) return OSF_ERR_CUDA;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const HostUnits h = host_units(dtype, B, Hq, Hkv, Sq, Sk, D);
+    char *base = static_cast<char *>(device_buffer);
+    char *dq = base + L.q, *dk = base + L.k, *dv = base + L.v, *dout = base + L.o;
+    void *ws = L.ws_bytes > 0 ? base + L.ws : nullptr;
+    const char *hq = static_cast<const char *>(Q), *hk = static_cast<const char *>(K),
+               *hv = static_cast<const char *>(V);
+    char *ho = static_cast<char *>(O);
+    const int G = Hq / Hkv;
+    // everything earlier on the caller's stream (a previous call using this buffer) comes first
+    if (cudaEventRecord(hs->start, s) != cudaSuccess || cudaStreamWaitEvent(hs->in, hs->start, 0) != cudaSuccess)
+        return OSF_ERR_CUDA;
+    for (int c = 0; c < h.chunks; ++c) {
+        const long long u0 = (long long)c * h.per;
+        const long long n = std::min<long long>(h.per, h.units - u0);
+        const size_t qo = (size_t)u0 * h.q_unit, ko = (size_t)u0 * h.kv_unit;
+        const size_t qn = (size_t)n * h.q_unit, kn = (size_t)n * h.kv_unit;
+        if (cudaMemcpyAsync(dq + qo, hq + qo, qn, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+            cudaMemcpyAsync(dk + ko, hk + ko, kn, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+            cudaMemcpyAsync(dv + ko, hv + ko, kn, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+            cudaEventRecord(hs->landed[c], hs->in) != cudaSuccess || cudaStreamWaitEvent(s, hs->landed[c], 0) != cudaSuccess)
+            return OSF_ERR_CUDA;
+        // the chunk as its own problem: B = n units, Hq = G, Hkv = 1
+        AttnProblem pc;
+        bool ec;
+        st = check_gqa(dq + qo, dk + ko, dv + ko, dout + qo, dtype, (int)n, G, 1, Sq, Sk, D, causal, scale, nullptr,
+                       pc, ec);
+        if (st != OSF_OK) return st;
+        const Path path = choose_path(pc, dq + qo, dk + ko, dv + ko, dout + qo);
+        st = run_gqa(pc, path, ws, L.ws_bytes, plan_splits(pc, path, dev->sm_count, 0), dev, s);
+        if (st != OSF_OK) return st;
+        if (cudaEventRecord(hs->computed[c], s) != cudaSuccess || cudaStreamWaitEvent(hs->out, hs->computed[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(ho + qo, dout + qo, qn, cudaMemcpyDeviceToHost, hs->out) != cudaSuccess)
+            return OSF_ERR_CUDA;
+    }
+    // the caller's stream continues once O has reached the host
+    if (cudaEventRecord(hs->done, hs->out) != cudaSuccess || cudaStreamWaitEvent(s, hs->done, 0) != cudaSuccess)
+        return OSF_ERR_CUDA;
+    return OSF_OK;
 }
 
 int osf_attn_decode_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sk, int D,

@@ -71,6 +71,24 @@ def test_invalid_arguments_rejected_on_host(osf):
     assert lib.osf_attn_workspace_bytes(1, 1, 3, 2, 1, 8, 64, ctypes.byref(n)) == osf.OSF_ERR_INVALID
 
 
+def test_host_buffer_entry_point_rejects_invalid_arguments_on_host(osf):
+    """osf_attn_fwd_gqa_host checks sizes, host pointers and its device buffer before any copy."""
+    lib = osf.lib()
+    p = ctypes.c_void_p(1 << 40)
+    o = ctypes.c_void_p(1 << 44)
+    buf = ctypes.c_void_p(1 << 45)
+    f = lib.osf_attn_fwd_gqa_host
+    args = lambda Hq, Hkv, Sq, Sk, causal, b: (p, p, p, o, 1, 1, Hq, Hkv, Sq, Sk, 64, causal, 0.0, b, 1 << 30, None)
+    assert f(*args(6, 4, 8, 8, 0, buf)) == osf.OSF_ERR_INVALID         # Hq % Hkv != 0
+    assert f(*args(4, 4, 8, 9, 1, buf)) == osf.OSF_ERR_INVALID         # causal with 1 < Sq != Sk
+    assert f(*args(4, 4, 0, 8, 0, None)) == osf.OSF_OK                 # empty: nothing to do
+    assert f(*args(4, 2, 8, 8, 0, None)) == osf.OSF_ERR_WORKSPACE      # no device buffer
+    assert f(p, p, p, p, 1, 1, 4, 4, 8, 8, 64, 0, 0.0, buf, 1 << 30, None) == osf.OSF_ERR_INVALID   # O overlaps Q
+    n = ctypes.c_size_t(7)
+    assert lib.osf_attn_host_buffer_bytes(1, 1, 6, 4, 8, 8, 64, 0, ctypes.byref(n)) == osf.OSF_ERR_INVALID
+    assert lib.osf_attn_host_buffer_bytes(1, 1, 4, 4, 8, 8, 64, 0, None) == osf.OSF_ERR_INVALID
+
+
 def test_strided_entry_point_rejects_bad_layouts_on_host(osf):
     """osf_attn_fwd_gqa_ex validates strides and masks before touching the device."""
     lib = osf.lib()
