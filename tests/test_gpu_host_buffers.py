@@ -88,3 +88,22 @@ def test_host_entry_point_rejects_small_buffer(osf):
     with pytest.raises(osf.OsfError) as e:
         osf.osf_attn_fwd_gqa_host(q, k, k.clone().pin_memory(), device_buffer=small)
     assert e.value.status == osf.OSF_ERR_WORKSPACE
+
+
+def test_host_entry_point_full_size_gqa_causal_prefill(osf):
+    """The GQA causal prefill workload (B=2, Hq=32, Hkv=8, S=4096, D=128, bf16) from pinned host
+    buffers, as the benchmark runs it: sampled rows of every head against the oracle, and the
+    whole output against the device-buffer entry point."""
+    B, Hq, Hkv, S, D = 2, 32, 8, 4096, 128
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=0, dtype="bf16")
+    out = osf.osf_attn_fwd_gqa_host(host(q, "bf16"), host(k, "bf16"), host(v, "bf16"), causal=True)
+    d = osf.osf_attn_fwd_gqa(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), causal=True)
+    torch.cuda.synchronize()
+    of = out.float().numpy()
+    diff = float(np.max(np.abs(of - d.float().cpu().numpy())))
+    assert diff <= 2e-2, f"host path differs from the device entry point by {diff}"
+    rng = np.random.default_rng(1)
+    rows = [(b, h, i) for b in range(B) for h in range(Hq)
+            for i in (0, 255, 256, S - 1, int(rng.integers(0, S)))]
+    ref, _ = oracle.attention_rows(f64(q, "bf16"), f64(k, "bf16"), f64(v, "bf16"), rows, causal=True)
+    assert_bf16_close(np.stack([of[b, h, i] for b, h, i in rows]), ref, "host path full size")
