@@ -88,19 +88,29 @@ SM_COUNT_GB300 = 152
 # each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
 # source that changed since the capture reports null.
 TRAFFIC = {
-    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
-                           "bytes": 136.32e6, "scope": "attn_tc_kernel<128>, one launch"},
-    "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "0be7a5998426353c",
-                   "bytes": 1079.08e6, "scope": "decode_kernel<128>, one launch"},
+    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
+                           "bytes": 136.66e6, "scope": "attn_tc_kernel<128>, one launch"},
+    "gqa_causal_prefill_bshd": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
+                                "bytes": 134.10e6, "scope": "attn_tc_kernel<128> on [B, S, H, D] views, one launch"},
+    "gqa_chunked_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
+                            "bytes": 52.07e6, "scope": "attn_tc_kernel<128>, bottom-right mask, one launch"},
+    "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "08ba6f0fc6b184f5",
+                   "bytes": 1079.13e6, "scope": "decode_kernel<128>, one launch"},
+    "gqa_speculative_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "08ba6f0fc6b184f5",
+                               "bytes": 1085.72e6, "scope": "decode_kernel<128>, 16 rows per kv head, one launch"},
     "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
                      "bytes": 1012.50e6, "scope": "softmax_rows_resident_kernel<8>, one launch"},
     "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
                    "bytes": 756.78e6, "scope": "step: chunk state + chunk normalise kernels"},
-    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "c0c998b1ef1451bf",
-                            "bytes": 521.27e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
-    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
-                             "bytes": 4.33e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
-    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "e045a11b681b4119",
+    "softmax_rows_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "3db986c55e395a29",
+                          "bytes": 476.42e6, "scope": "softmax_ex_smem_kernel<bf16, bf16, 256>, one launch"},
+    "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "3db986c55e395a29",
+                            "bytes": 343.78e6, "scope": "softmax_ex_smem_kernel<bf16, bf16, 64>, one launch"},
+    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "0c7cd58496abe167",
+                            "bytes": 521.73e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
+    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
+                             "bytes": 4.34e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
+    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
                               "bytes": 1.63e6, "scope": "attn_tc_kernel<64>, one launch (8 key splits)"},
 }
 
