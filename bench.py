@@ -15,7 +15,7 @@ Barrier + synchronize on both sides of the timed loop; the max over ranks is rep
 With torchrun (N > 1) every rank runs its own replica of the workload (weak scaling: the
 path shards over (batch, kv head) with no exchange).
 
---impl reference times the fp64 CPU oracle (the reference arm of this build) on a bounded
+--impl reference times the fp64 CPU oracle (the reference arm) on a bounded
 sample of the same workload, on the host cores.
 """
 from __future__ import annotations
