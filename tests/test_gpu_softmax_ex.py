@@ -66,6 +66,20 @@ def test_causal_scaled_attention_weights(osf, dtype, Sq, heads):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,T,period", [(2048, 2048, 2048), (3000, 2048, 1500), (500, 4096, 100000),
+                                           (1000, 8192, 333)])
+def test_causal_periods_long_rows(osf, dtype, rows, T, period):
+    """Causal rows long enough that the rows keeping at most half their columns run with half the
+    row buffer: whole and partial periods, a period longer than the rows, and one shorter than T."""
+    x32 = (si.normal_f32((rows, T), rows + T, si.STREAM_X) * 9).astype(np.float32)
+    x = to_dev(x32, dtype)
+    z = osf.osf_softmax_rows_ex(x, scale=0.3, causal_period=period)
+    ref = oracle.softmax_masked(values(x), 0.3, period)
+    check(z, ref, f"causal {dtype} rows={rows} T={T} period={period}")
+    assert np.all(values(z)[ref == 0] == 0), "masked columns must be exactly zero"
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_padded_row_strides_and_in_place(osf, dtype):
     x32 = si.softmax_rows_input(40, 1000, seed=5)
     x = to_dev(x32, dtype, pad=24)          # row stride 1024: aligned
