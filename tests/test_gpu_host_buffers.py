@@ -107,3 +107,36 @@ def test_host_entry_point_full_size_gqa_causal_prefill(osf):
             for i in (0, 255, 256, S - 1, int(rng.integers(0, S)))]
     ref, _ = oracle.attention_rows(f64(q, "bf16"), f64(k, "bf16"), f64(v, "bf16"), rows, causal=True)
     assert_bf16_close(np.stack([of[b, h, i] for b, h, i in rows]), ref, "host path full size")
+
+
+def test_host_entry_point_concurrent_threads(osf):
+    """Calls from two host threads at once, each on its own stream and device buffer (the library
+    serialises their enqueueing on the shared copy streams): both results match the oracle."""
+    import threading
+    B, Hq, Hkv, S, D = 1, 8, 2, 384, 128
+    cases = []
+    for seed in (21, 22):
+        q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=seed, dtype="bf16")
+        cases.append((host(q, "bf16"), host(k, "bf16"), host(v, "bf16"),
+                      oracle.attention_gqa(f64(q, "bf16"), f64(k, "bf16"), f64(v, "bf16"), causal=True)[0]))
+    outs = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(3):
+                    outs[i] = osf.osf_attn_fwd_gqa_host(*cases[i][:3], causal=True)
+            st.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        assert_bf16_close(outs[i].float().numpy(), cases[i][3], f"thread {i}")
