@@ -339,15 +339,27 @@ int host_streams(HostStreams **out) {
     if (current_device(&dev) != OSF_OK) return OSF_ERR_CUDA;
     HostStreams &h = g_host[dev];
     if (!h.ready) {
-        if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) != cudaSuccess)
+        bool ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; ok && i < kHostChunks; ++i)
+            ok = cudaEventCreateWithFlags(&h.landed[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.computed[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            // release what was created, so a later call starts over cleanly
+            if (h.in) cudaStreamDestroy(h.in);
+            if (h.out) cudaStreamDestroy(h.out);
+            cudaEvent_t *evs[] = {&h.start, &h.done};
+            for (cudaEvent_t *e : evs)
+                if (*e) cudaEventDestroy(*e);
+            for (int i = 0; i < kHostChunks; ++i) {
+                if (h.landed[i]) cudaEventDestroy(h.landed[i]);
+                if (h.computed[i]) cudaEventDestroy(h.computed[i]);
+            }
+            h = HostStreams();
             return OSF_ERR_CUDA;
-        for (int i = 0; i < kHostChunks; ++i)
-            if (cudaEventCreateWithFlags(&h.landed[i], cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&h.computed[i], cudaEventDisableTiming) != cudaSuccess)
-                return OSF_ERR_CUDA;
+        }
         h.ready = true;
     }
     *out = &h;
