@@ -134,3 +134,22 @@ def test_product_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "seeded_inputs" not in src, f
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/osf.h compiles as C99 on its own (no CUDA or torch headers needed by a caller)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_osf.c"
+    src.write_text('#include <stdio.h>\n#include "osf.h"\n'
+                   "int use(void *q, void *k, void *v, void *o, void *ws, size_t n, osf_stream s) {\n"
+                   "    int st = osf_attn_fwd_gqa(q, k, v, o, OSF_BF16, 2, 32, 8, 4096, 4096, 128, 1, 0.f,\n"
+                   "                              NULL, ws, n, s);\n"
+                   "    if (st != OSF_OK) fprintf(stderr, \"%s\\n\", osf_status_string(st));\n"
+                   "    return st;\n}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
