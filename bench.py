@@ -4,8 +4,15 @@
 One JSON line on stdout (rank 0).  Default workload: the batched GQA causal prefill
 (B=2, Hq=32, Hkv=8, Sq=Sk=4096, D=128, bf16), whose bf16 tensor-core throughput is the headline
 attention metric; the other workloads (single-head fp32/bf16 4096x4096 d=64, the M=64 N=100
-d=32 single head, split-K decode, row softmax, 1-D softmax) are measured after it in the same
-run and reported under "suite".
+d=32 single head, split-K decode, row softmax, 1-D softmax, and the "next" rows) are measured
+after it in the same run and reported under "suite", the last key of the line, each as a short
+object (value, unit, ms per step, roofline bound / peak / fraction / ncu DRAM bytes, and for the
+problem statement's configurations the oracle's throughput on all host cores and on one core).
+The full suite entries go to stderr, one JSON object per line.
+
+cpu_baseline: the fp64 oracle on a bounded sample of the headline workload, on all host cores,
+and under "one_core" in a child process pinned to one core with one BLAS thread (its
+"full_workload_s" extrapolates the sample's rate to the whole workload).
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA events on the
 launching stream; between timed steps, outside the events, L2 is flushed by writing a 512 MiB
@@ -458,13 +465,24 @@ def roofline(res, pk, w):
 
 
 # ------------------------------------------------------------------------------ oracle arm
+def host_cores():
+    """Host cores this process may run on (numpy's BLAS starts one thread per core)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def oracle_timed(name, w, budget_s):
-    """Like oracle_sample but with input generation outside the clock."""
+    """Oracle throughput on a bounded sample of a workload: `budget_s` seconds of oracle time,
+    input generation outside the clock (and the whole loop capped at four times the budget)."""
     import oracle
     import seeded_inputs as si
     amount, unit, _ = work_units(w)
-    cores = os.cpu_count() or 1
+    cores = host_cores()
     elapsed, done, n = 0.0, 0.0, 0
+    wall0 = time.perf_counter()
+    budget_left = lambda: elapsed < budget_s and time.perf_counter() - wall0 < 4 * budget_s
     if w["kind"] == "solve":
         Q, K, V = make_inputs(name, w)
         while elapsed < min(budget_s, 2.0):
@@ -477,7 +495,7 @@ def oracle_timed(name, w, budget_s):
     if w["kind"] == "attn_bwd":
         B, Hq, S, D = w["B"], w["Hq"], w["Sq"], w["D"]
         per_head = amount / (B * Hq)
-        while n < B * Hq and elapsed < budget_s:
+        while n < B * Hq and budget_left():
             q, kk, vv, g = (si.normal_f32((S, D), n, st) for st in (si.STREAM_Q, si.STREAM_K, si.STREAM_V, si.STREAM_X))
             q, kk, vv, g = (si.bf16_bits_to_f32(si.f32_to_bf16_bits(a)) for a in (q, kk, vv, g))
             t = time.perf_counter()
@@ -489,7 +507,7 @@ def oracle_timed(name, w, budget_s):
     if w["kind"] == "attn" and w["Sq"] > 1:
         B, Hq, S, D = w["B"], w["Hq"], w["Sq"], w["D"]
         per_head = amount / (B * Hq)
-        while n < B * Hq and elapsed < budget_s:
+        while n < B * Hq and budget_left():
             q = si.normal_f32((S, D), n, si.STREAM_Q)
             kk = si.normal_f32((w["Sk"], D), n, si.STREAM_K)
             vv = si.normal_f32((w["Sk"], D), n, si.STREAM_V)
@@ -508,7 +526,7 @@ def oracle_timed(name, w, budget_s):
         B, Hq, Hkv, Sk, D = w["B"], w["Hq"], w["Hkv"], w["Sk"], w["D"]
         G = Hq // Hkv
         per = amount / (B * Hkv)
-        while n < B * Hkv and elapsed < budget_s:
+        while n < B * Hkv and budget_left():
             q = si.normal_f32((1, G, 1, D), n, si.STREAM_Q)
             kk = si.normal_f32((1, 1, Sk, D), n, si.STREAM_K)
             vv = si.normal_f32((1, 1, Sk, D), n, si.STREAM_V)
@@ -521,7 +539,7 @@ def oracle_timed(name, w, budget_s):
     rows, T = w["rows"], w["T"]
     P = w.get("period", 0)
     step = P if P else (64 if rows > 1 else 1)   # whole score matrices keep the causal row numbers
-    while n < rows and elapsed < budget_s:
+    while n < rows and budget_left():
         x = si.softmax_rows_input(step, T, n)
         if w.get("dtype") == "bf16":
             x = si.bf16_bits_to_f32(si.f32_to_bf16_bits(x))
@@ -534,6 +552,54 @@ def oracle_timed(name, w, budget_s):
         n += step
         done += amount * step / rows
     return done / elapsed, unit, f"{n} of {rows} rows of {T}", cores
+
+
+# Thread-count variables of the BLAS libraries numpy may be built on.
+ONE_THREAD_ENV = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                                  "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS")}
+
+
+def oracle_probe(name, budget_s):
+    """Child-process side of `oracle_one_core`: pin this process to one core, time the oracle and
+    print one JSON object.  The BLAS thread variables were set before numpy was imported."""
+    try:
+        cpu = min(os.sched_getaffinity(0))
+        os.sched_setaffinity(0, {cpu})
+    except (AttributeError, OSError):
+        pass
+    v, unit, sample, _ = oracle_timed(name, WORKLOADS[name], budget_s)
+    print(json.dumps({"value": v, "unit": unit, "sample": sample, "cores": host_cores()}), flush=True)
+    return 0
+
+
+def oracle_one_core(name, budget_s):
+    """The oracle timed on ONE host core: a child process with one BLAS thread, pinned to one
+    core (`oracle_probe`).  None when the child fails."""
+    env = dict(os.environ, **ONE_THREAD_ENV)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-probe", name, "--cpu-budget", str(budget_s)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=30 + 6 * budget_s)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except (subprocess.SubprocessError, OSError, ValueError, IndexError):
+        return None
+
+
+# The configurations the metric is quoted on (one per problem statement item); the others are the
+# "next" rows.  Their oracle is timed on all host cores and on one core beside the GPU number.
+BASELINE_CONFIGS = ("single_head_m64_n100", "single_head_4096_f32", "single_head_4096_bf16", "gqa_causal_prefill",
+                    "gqa_decode", "softmax_rows", "softmax_1d")
+
+
+def compact(entry, oracle=None):
+    """A suite entry as a short object: value, unit, ms per step, and the roofline (bound, peak,
+    achieved fraction of it, DRAM bytes per launch from ncu or null); `oracle`: the oracle's
+    throughput in the same unit, [on all host cores, on one core]."""
+    rl = entry["roofline"]
+    out = {"v": entry["value"], "u": entry["unit"], "ms": entry["ms_per_step"],
+           "rl": {"bound": rl["bound"], "peak": rl["peak"], "frac": rl["frac"], "dram": rl["traffic"]}}
+    if oracle:
+        out["oracle"] = oracle
+    return out
 
 
 # ------------------------------------------------------------------------------ main
@@ -599,7 +665,12 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds per reference-arm step")
     ap.add_argument("--rows", type=int, default=0,
                     help="row count of a softmax workload instead of its own (a smaller case to profile)")
+    ap.add_argument("--suite-oracle-budget", type=float, default=2.5,
+                    help="seconds of oracle time per suite configuration (all cores, then one core)")
+    ap.add_argument("--oracle-probe", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_probe:
+        return oracle_probe(args.oracle_probe, args.cpu_budget)
     if args.rows:
         w0 = WORKLOADS[args.workload]
         if w0["kind"] != "softmax" or args.rows < 1:
@@ -652,9 +723,26 @@ def main():
                            "device_status": r2["status"]}
 
     cpu = None
+    suite_oracle = {}
     if rank == 0:
         v, unit, sample, cores = oracle_timed(args.workload, w, args.cpu_budget)
         cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+        one = oracle_one_core(args.workload, args.cpu_budget)
+        if one:
+            one["full_workload_s"] = round(res["amount"] / one["value"], 1)   # one core, extrapolated
+            cpu["one_core"] = one
+        if not args.no_suite:
+            for name in BASELINE_CONFIGS:
+                if name not in suite:
+                    continue
+                a = oracle_timed(name, WORKLOADS[name], args.suite_oracle_budget)
+                o = oracle_one_core(name, args.suite_oracle_budget)
+                # [all host cores (cpu_baseline.cores of them), one core]
+                suite_oracle[name] = [float(f"{a[0]:.4g}"), float(f"{o['value']:.4g}") if o else None]
+        # the full suite entries, one line each, on stderr (stdout carries the one result line)
+        for name, e in suite.items():
+            print(json.dumps({"suite_entry": name, **e, "oracle": suite_oracle.get(name)}), file=sys.stderr,
+                  flush=True)
 
     if rank == 0:
         line = {
@@ -670,7 +758,9 @@ def main():
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                     "ms_per_step": round(e2e_ms, 5), "call": res["e2e_call"]},
             "gpu_launches": res["launches"], "launches_per_step": res["launches_per_call"],
-            "device_status": res["status"], "clocks": sampler.summary(), "suite": suite,
+            "device_status": res["status"], "clocks": sampler.summary(),
+            # last, and short, so that the end of the line holds every workload's number
+            "suite": {n: compact(e, suite_oracle.get(n)) for n, e in suite.items()},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

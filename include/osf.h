@@ -112,8 +112,11 @@ int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int d
  * workspace: osf_attn_bwd_workspace_bytes bytes (one float per query row).
  * dQ, dK, dV must not overlap one another or any input -> else OSF_ERR_INVALID.
  * B, Sq or Sk == 0: OSF_OK, nothing written.  Other errors as in osf_attn_fwd_gqa.
- * Kernel choice: bf16 with D in {64, 128} (16-byte aligned pointers) runs warp-level
- * tensor-core kernels; everything else a CUDA-core kernel with one warp per row.
+ * Kernel choice: bf16 with D in {64, 128} whose tensors TMA can address (16-byte aligned
+ * pointers) runs a row-sum pre-pass and then one grid of tcgen05 tensor-core CTAs (dK/dV CTAs
+ * per key tile, dQ CTAs per query tile; accumulators in TMEM, tiles streamed by TMA); other
+ * bf16 D in {64, 128} cases the warp-level mma.sync kernels; everything else a CUDA-core kernel
+ * with one warp per row.
  */
 int osf_attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                      const float *lse, void *dQ, void *dK, void *dV, int dtype, int B, int Hq, int Hkv,
@@ -179,6 +182,9 @@ int osf_attn_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, 
  * reached the host: synchronise `stream` before reading O.  The first call on a device creates
  * the two copy streams and their events (kept until exit); calls are serialised while they
  * enqueue.  lse is not produced.  Sizes, errors and emptiness as in osf_attn_fwd_gqa.
+ * After a non-OK return the contents of O are undefined (some chunks may have been copied back,
+ * others not); `stream` is still ordered after every copy and kernel the call had queued, so
+ * work enqueued on it afterwards, or a synchronisation of it, waits for them.
  */
 int osf_attn_fwd_gqa_host(const void *Q, const void *K, const void *V, void *O, int dtype,
                           int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,

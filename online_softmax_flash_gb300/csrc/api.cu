@@ -80,6 +80,18 @@ int device_info(DeviceInfo **out) {
     return OSF_OK;
 }
 
+}  // namespace
+
+int device_sm_count(int *sms) {
+    DeviceInfo *d;
+    const int st = device_info(&d);
+    if (st != OSF_OK) return st;
+    *sms = d->sm_count;
+    return OSF_OK;
+}
+
+namespace {
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     if (!a || !b || na == 0 || nb == 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -511,6 +523,15 @@ int osf_attn_fwd_gqa_host(const void *Q, const void *K, const void *V, void *O, 
     // everything earlier on the caller's stream (a previous call using this buffer) comes first
     if (cudaEventRecord(hs->start, s) != cudaSuccess || cudaStreamWaitEvent(hs->in, hs->start, 0) != cudaSuccess)
         return OSF_ERR_CUDA;
+    // On an error after this point some chunks may already be queued on the copy streams: the
+    // caller's stream is made to wait for both of them (best effort) so that work it enqueues
+    // next still runs after them, and the error is returned.  O is then undefined.
+    auto fail = [&](int code) {
+        if (cudaEventRecord(hs->start, hs->in) == cudaSuccess) cudaStreamWaitEvent(s, hs->start, 0);
+        if (cudaEventRecord(hs->done, hs->out) == cudaSuccess) cudaStreamWaitEvent(s, hs->done, 0);
+        cudaGetLastError();
+        return code;
+    };
     for (int c = 0; c < h.chunks; ++c) {
         const long long u0 = (long long)c * h.per;
         const long long n = std::min<long long>(h.per, h.units - u0);
@@ -520,23 +541,23 @@ int osf_attn_fwd_gqa_host(const void *Q, const void *K, const void *V, void *O, 
             cudaMemcpyAsync(dk + ko, hk + ko, kn, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
             cudaMemcpyAsync(dv + ko, hv + ko, kn, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
             cudaEventRecord(hs->landed[c], hs->in) != cudaSuccess || cudaStreamWaitEvent(s, hs->landed[c], 0) != cudaSuccess)
-            return OSF_ERR_CUDA;
+            return fail(OSF_ERR_CUDA);
         // the chunk as its own problem: B = n units, Hq = G, Hkv = 1
         AttnProblem pc;
         bool ec;
         st = check_gqa(dq + qo, dk + ko, dv + ko, dout + qo, dtype, (int)n, G, 1, Sq, Sk, D, causal, scale, nullptr,
                        pc, ec);
-        if (st != OSF_OK) return st;
+        if (st != OSF_OK) return fail(st);
         const Path path = choose_path(pc, dq + qo, dk + ko, dv + ko, dout + qo);
         st = run_gqa(pc, path, ws, L.ws_bytes, plan_splits(pc, path, dev->sm_count, 0), dev, s);
-        if (st != OSF_OK) return st;
+        if (st != OSF_OK) return fail(st);
         if (cudaEventRecord(hs->computed[c], s) != cudaSuccess || cudaStreamWaitEvent(hs->out, hs->computed[c], 0) != cudaSuccess ||
             cudaMemcpyAsync(ho + qo, dout + qo, qn, cudaMemcpyDeviceToHost, hs->out) != cudaSuccess)
-            return OSF_ERR_CUDA;
+            return fail(OSF_ERR_CUDA);
     }
     // the caller's stream continues once O has reached the host
     if (cudaEventRecord(hs->done, hs->out) != cudaSuccess || cudaStreamWaitEvent(s, hs->done, 0) != cudaSuccess)
-        return OSF_ERR_CUDA;
+        return fail(OSF_ERR_CUDA);
     return OSF_OK;
 }
 

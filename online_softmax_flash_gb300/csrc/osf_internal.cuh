@@ -90,6 +90,10 @@ __host__ __device__ __forceinline__ long long o_at(const AttnProblem &p, int b, 
     return b * p.o_sb + h * p.o_sh + s * p.o_ss;
 }
 
+// SM count of the current device, looked up once per device (the same value every entry point
+// sizes its grids and workspaces with).  Returns an osf_status.
+int device_sm_count(int *sms);
+
 // Count of kernels launched by the library (diagnostics; see osf_launch_count).
 void count_launches(int n);
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device.  The attribute

@@ -24,30 +24,21 @@ constexpr long long kNoAllocMaxStates = 16384;
 
 static __device__ __align__(256) float2 g_noalloc_scratch[kNoAllocMaxStates];
 
-struct NoAllocDevice {
-    float *scratch = nullptr;   // device address of g_noalloc_scratch on this device
-    int sm_count = 0;
-};
-NoAllocDevice g_na_dev[kNoAllocMaxDevices];
+float *g_na_scratch[kNoAllocMaxDevices];   // device address of g_noalloc_scratch, per device
 std::mutex g_na_mutex;
 
 // One-time set-up per device, with that device current: the array's device address (in host
-// code its name is only a host-side stand-in, never a usable pointer) and the SM count.
-int noalloc_setup(NoAllocDevice **out) {
+// code its name is only a host-side stand-in, never a usable pointer).
+int noalloc_scratch(float **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return OSF_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_na_mutex);
-    NoAllocDevice &d = g_na_dev[dev];
-    if (!d.scratch) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-            return OSF_ERR_CUDA;
+    if (!g_na_scratch[dev]) {
         float *ptr = nullptr;
         if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return OSF_ERR_CUDA;
-        d.sm_count = sms;
-        d.scratch = ptr;
+        g_na_scratch[dev] = ptr;
     }
-    *out = &d;
+    *out = g_na_scratch[dev];
     return OSF_OK;
 }
 
@@ -64,11 +55,16 @@ extern "C" int osf_softmax_rows_noalloc(const float *x, float *z, long long rows
     const size_t n = (size_t)rows * (size_t)T * sizeof(float);
     const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(z);
     if (a != b && a < b + n && b < a + n) return OSF_ERR_INVALID;  // partial overlap
-    NoAllocDevice *d = nullptr;
-    const int st = noalloc_setup(&d);
+    // the SM count every entry point uses: the capacity check and the launch geometry agree
+    // with osf_softmax_rows
+    int sms = 0;
+    int st = device_sm_count(&sms);
     if (st != OSF_OK) return st;
-    const size_t states = softmax_workspace_floats(rows, T, d->sm_count) / 2;
+    float *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != OSF_OK) return st;
+    const size_t states = softmax_workspace_floats(rows, T, sms) / 2;
     if ((long long)states > kNoAllocMaxStates) return OSF_ERR_WORKSPACE;
-    return launch_softmax_rows(x, z, rows, T, d->scratch, d->sm_count, (cudaStream_t)stream) == cudaSuccess
-               ? OSF_OK : OSF_ERR_CUDA;
+    return launch_softmax_rows(x, z, rows, T, scratch, sms, (cudaStream_t)stream) == cudaSuccess ? OSF_OK
+                                                                                                  : OSF_ERR_CUDA;
 }

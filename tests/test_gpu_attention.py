@@ -93,9 +93,10 @@ def test_gqa_small(osf, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
     assert_f32_close(lse.cpu().numpy(), ref_lse, atol=1e-3, what="lse")
 
 
-def test_gqa_causal_prefill_full_size_sampled(osf):
-    """The GQA causal prefill workload at full size (B=2, Hq=32, Hkv=8, S=4096, D=128, bf16),
-    checked at sampled rows (first/last rows, tile edges, random rows) on every head."""
+def test_gqa_causal_prefill_full_size(osf):
+    """The GQA causal prefill workload at full size (B=2, Hq=32, Hkv=8, S=4096, D=128, bf16), in
+    the launch configuration the benchmark times: every output element and every lse against the
+    oracle (64 heads of explicit 4096 x 4096 fp64 scores), and two calls bit-identical."""
     B, Hq, Hkv, S, D = 2, 32, 8, 4096, 128
     q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=0, dtype="bf16")
     lse = torch.empty(B, Hq, S, device="cuda")
@@ -103,20 +104,9 @@ def test_gqa_causal_prefill_full_size_sampled(osf):
     o2 = osf.osf_attn_fwd_gqa(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o, o2), "two identical calls differ"
-    rng = np.random.default_rng(0)
-    rows = []
-    for b in range(B):
-        for h in range(Hq):
-            for i in (0, 1, 127, 128, 255, 256, S - 129, S - 128, S - 1, int(rng.integers(0, S))):
-                rows.append((b, h, i))
-    qf, kf, vf = (si.bf16_bits_to_f32(a) for a in (q, k, v))
-    ref, ref_lse = oracle.attention_rows(qf, kf, vf, rows, causal=True)
-    of = o.float().cpu().numpy()
-    got = np.stack([of[b, h, i] for b, h, i in rows])
-    assert_bf16_close(got, ref, "gqa prefill full size")
-    lf = lse.cpu().numpy()
-    assert_f32_close(np.array([lf[b, h, i] for b, h, i in rows]), ref_lse, atol=1e-3, what="lse")
-    assert torch.isfinite(o.float()).all()
+    ref, ref_lse = oracle.attention_gqa(*(si.bf16_bits_to_f32(a) for a in (q, k, v)), causal=True)
+    assert_bf16_close(o.float().cpu().numpy(), ref, "gqa prefill full size, every element")
+    assert_f32_close(lse.cpu().numpy(), ref_lse, atol=1e-3, what="lse, every row")
 
 
 @pytest.mark.parametrize("causal", [True, False])

@@ -94,10 +94,11 @@ def test_padded_row_strides_and_in_place(osf, dtype):
     check(w, ref, f"in place {dtype}")
 
 
-def test_bf16_rows_full_size_sampled(osf):
-    """The softmax workload shape (4096 x 32768) in bf16 in and out, checked on sampled rows."""
+def test_bf16_rows_full_size(osf):
+    """The softmax workload shape (4096 x 32768) in bf16 in and out, as the benchmark runs it:
+    every row against the oracle (compared in blocks of rows to bound host memory)."""
     rows, T = 4096, 32768
     x = torch.from_numpy(si.softmax_rows_input(rows, T, seed=0)).cuda().to(torch.bfloat16)
     z = osf.osf_softmax_rows_ex(x)
-    pick = [0, 1, 2047, 4095] + list(range(17, rows, 509))
-    check(z[pick], oracle.softmax_masked(values(x[pick])), "bf16 4096x32768 sampled")
+    for r0 in range(0, rows, 512):
+        check(z[r0:r0 + 512], oracle.softmax_masked(values(x[r0:r0 + 512])), f"bf16 4096x32768 rows {r0}+")

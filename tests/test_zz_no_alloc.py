@@ -1,18 +1,20 @@
-"""osf_softmax_rows_noalloc, called through the C ABI, against osf_softmax_rows.
+"""osf_softmax_rows_noalloc, called through the C ABI, against the oracle and osf_softmax_rows.
 
 The no-allocation entry point serves callers that cannot call cudaMalloc (for example code
 running during CUDA graph capture, or a library given only its input and output buffers).  It
-must give the same result as the workspace-taking entry point, on two calls in a row (the
-shared scratch array keeps the previous call's contents), and refuse problems larger than its
-fixed scratch.  This file is collected last so a failure here cannot hide earlier tests.
+must give the same result as the workspace-taking entry point and as the fp64 oracle, on two
+calls in a row (the shared scratch array keeps the previous call's contents), and refuse problems
+larger than its fixed scratch.  This file is collected last so a failure here cannot hide
+earlier tests.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import seeded_inputs as si
-from conftest import F32_ATOL, SUM_TOL, f32_tensor
+from conftest import F32_ATOL, SUM_TOL, assert_f32_close, f32_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -27,31 +29,59 @@ def noalloc_fn(osf):
 
 
 @pytest.mark.parametrize("rows,T", [(1, 1 << 22), (3, 100003), (7, 32768), (2, 40001)])
-def test_noalloc_matches_workspace_entry_point(osf, rows, T):
+def test_noalloc_matches_oracle_and_workspace_entry_point(osf, rows, T):
     fn = noalloc_fn(osf)
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):   # two calls in a row: the shared scratch holds the previous call's states
-        x = f32_tensor(si.softmax_rows_input(rows, T, seed=100 * call + rows))
+        xh = si.softmax_rows_input(rows, T, seed=100 * call + rows)
+        x = f32_tensor(xh)
         ref = osf.osf_softmax_rows(x)
         z = torch.full_like(x, float("nan"))
         st = fn(x.data_ptr(), z.data_ptr(), rows, T, stream)
         assert st == osf.OSF_OK, osf.osf_status_string(st)
         torch.cuda.synchronize()
+        got = z.cpu().numpy()
+        assert_f32_close(got, oracle.softmax(xh), what=f"call {call} against the oracle")
         diff = float((z - ref).abs().max())
-        assert diff <= F32_ATOL, f"call {call}: max abs difference {diff:.3e}"
-        sums = z.double().sum(dim=-1).cpu().numpy()
+        assert diff <= F32_ATOL, f"call {call}: max abs difference {diff:.3e} to osf_softmax_rows"
+        sums = got.astype(np.float64).sum(axis=-1)
         assert float(np.max(np.abs(sums - 1.0))) <= SUM_TOL
     assert osf.osf_device_status() == osf.OSF_OK
 
 
 def test_noalloc_in_place(osf):
     fn = noalloc_fn(osf)
-    x = f32_tensor(si.softmax_rows_input(1, 1 << 20, seed=5))
-    ref = osf.osf_softmax_rows(x)
+    xh = si.softmax_rows_input(1, 1 << 20, seed=5)
+    x = f32_tensor(xh)
     st = fn(x.data_ptr(), x.data_ptr(), 1, 1 << 20, torch.cuda.current_stream().cuda_stream)
     assert st == osf.OSF_OK
     torch.cuda.synchronize()
-    assert float((x - ref).abs().max()) <= F32_ATOL
+    assert_f32_close(x.cpu().numpy(), oracle.softmax(xh), what="in place")
+
+
+@pytest.mark.parametrize("rows,T", [(1, 1 << 22), (3, 100003)])
+def test_noalloc_captured_in_a_graph(osf, rows, T):
+    """The documented use: one eager call first (it looks up the array on this device), then the
+    entry point inside a captured CUDA graph, whose replay must equal the eager result bit for bit
+    (the kernels are deterministic)."""
+    fn = noalloc_fn(osf)
+    x = f32_tensor(si.softmax_rows_input(rows, T, seed=77))
+    z = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        assert fn(x.data_ptr(), z.data_ptr(), rows, T, side.cuda_stream) == osf.OSF_OK
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = z.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = fn(x.data_ptr(), z.data_ptr(), rows, T, torch.cuda.current_stream().cuda_stream)
+    assert st == osf.OSF_OK
+    z.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager, z)
 
 
 def test_noalloc_rejects_oversize_and_bad_arguments(osf):
