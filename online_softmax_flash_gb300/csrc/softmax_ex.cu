@@ -9,8 +9,9 @@
 // Values are converted to fp32 on load; exponentials are base 2 on x * scale * log2(e).
 //
 // Paths: a row of at most 72 KB whose start and stride are 16-byte aligned is staged in shared
-// memory by one bulk copy (up to its causal limit) for a 256-thread CTA, so several rows are in
-// flight per SM and one row's load overlaps the others' arithmetic; other rows of up to 32768
+// memory by bulk copies (up to its causal limit; two pieces beyond 16 KB) for a CTA of 64-256
+// threads, so several rows are in flight per SM and one row's load overlaps the others'
+// arithmetic; other rows of up to 32768
 // elements are held in registers by one CTA of up to 1024 threads (one read, one write per
 // element; columns past lim are not read); unaligned short rows stream twice through one CTA;
 // longer rows are cut into chunks over the whole GPU (chunk states, then merge + normalise).
@@ -162,58 +163,81 @@ softmax_ex_onchip_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs
 }
 
 // One CTA of NT threads per row (256; 128 for rows of at most 16 KB and 64 for at most 8 KB,
-// so more rows are in flight per SM); the row (up to its causal limit, rounded up to 16 bytes) is copied into
-// shared memory by one bulk copy, then read twice from there: (m, l), then z.
+// so more rows are in flight per SM); the row (up to its causal limit, rounded up to 16 bytes) is
+// copied into shared memory by NP bulk copies of consecutive pieces, each completing on its own
+// mbarrier, then read twice from there: (m, l), folded piece by piece as the pieces land, then z.
+// Rows of more than 16 KB take two pieces, so the first half's (m, l) pass overlaps the second
+// half's copy (measured on GB300: 64 KB bf16 rows 5826 against 5579 GB/s with one piece; 4 or 8
+// pieces, or a 512-thread CTA, were slower; shorter rows gain nothing from pieces).
 constexpr uint32_t kSmemRowBytes = 72 * 1024;
 
-template <typename Tin, typename Tout, int NT>
+template <typename Tin, typename Tout, int NT, int NP>
 __global__ void __launch_bounds__(NT)
 softmax_ex_smem_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, long long zs, float mult,
                        long long period, int *status) {
     constexpr int E = Vec<Tin>::E;
     extern __shared__ __align__(16) uint8_t srow[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar[NP];
     __shared__ float sh[64];
     const long long row = blockIdx.x;
     const Tin *xr = x + row * xs;
     Tout *zr = z + row * zs;
     const int lim = (int)row_limit(row, T, period);
     const int nload = (lim + E - 1) / E;                 // 16-byte vectors copied
+    const int per = (nload + NP - 1) / NP;               // vectors per piece (the last may have fewer)
     const uint32_t sbuf = ptx::smem_u32(srow);
     if (threadIdx.x == 0) {
-        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) ptx::mbar_init(ptx::smem_u32(&bar[q]), 1);
         ptx::mbar_init_fence();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        ptx::mbar_expect_tx(ptx::smem_u32(&bar), (uint32_t)nload * 16u);
-        ptx::bulk_load(sbuf, xr, (uint32_t)nload * 16u, ptx::smem_u32(&bar));
-    }
-    bool ok = ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr);
-    if (!__syncthreads_and(ok)) {
-        // the copy never completed: record it, give it a bounded chance to land, leave
-        if (threadIdx.x == 0) atomicExch(status, kStatusTimeout);
-        ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr, 20000000ull);
-        return;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const int v0 = q * per, n = min(per, nload - v0);
+            if (n > 0) {
+                ptx::mbar_expect_tx(ptx::smem_u32(&bar[q]), (uint32_t)n * 16u);
+                ptx::bulk_load(sbuf + (uint32_t)v0 * 16u, xr + (long long)v0 * E, (uint32_t)n * 16u,
+                               ptx::smem_u32(&bar[q]));
+            }
+        }
     }
     const Tin *sx = reinterpret_cast<const Tin *>(srow);
     float m = -INFINITY, l = 0.f;
-    for (int i = threadIdx.x; i < nload; i += NT) {
-        float f[E];
-        Vec<Tin>::load_shared(sx + i * E, f);
-        float mx = -INFINITY;
+    bool ok = true;
+#pragma unroll 1
+    for (int q = 0; q < NP; ++q) {
+        const int v0 = q * per, v1 = min(nload, v0 + per);
+        if (v1 <= v0) break;
+        ok = ok && ptx::mbar_wait(ptx::smem_u32(&bar[q]), 0, nullptr);
+        if (!ok) break;
+        for (int i = v0 + threadIdx.x; i < v1; i += NT) {
+            float f[E];
+            Vec<Tin>::load_shared(sx + i * E, f);
+            float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            f[e] = (i * E + e < lim) ? f[e] * mult : -INFINITY;
-            mx = fmaxf(mx, f[e]);
+            for (int e = 0; e < E; ++e) {
+                f[e] = (i * E + e < lim) ? f[e] * mult : -INFINITY;
+                mx = fmaxf(mx, f[e]);
+            }
+            const float mn = fmaxf(m, mx);
+            const float mr = (mn == -INFINITY) ? 0.f : mn;
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) s += ex2_approx(f[e] - mr);
+            l = l * ex2_approx(m - mr) + s;
+            m = mn;
         }
-        const float mn = fmaxf(m, mx);
-        const float mr = (mn == -INFINITY) ? 0.f : mn;
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) s += ex2_approx(f[e] - mr);
-        l = l * ex2_approx(m - mr) + s;
-        m = mn;
+    }
+    if (!__syncthreads_and(ok)) {
+        // a copy never completed: record it, give the copies a bounded chance to land, leave
+        if (threadIdx.x == 0) {
+            atomicExch(status, kStatusTimeout);
+            for (int q = 0; q < NP; ++q) ptx::mbar_wait(ptx::smem_u32(&bar[q]), 0, nullptr, 20000000ull);
+        }
+        __syncthreads();
+        return;
     }
     cta_merge_ml(m, l, sh);
     const float mref = (m == -INFINITY) ? 0.f : m;
@@ -230,6 +254,102 @@ softmax_ex_smem_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, 
             for (int e = 0; e < E; ++e) f[e] = 0.f;
         }
         store_vec<E>(zr + (long long)i * E, f);
+    }
+}
+
+// Causal rows, two per CTA: rows i and P - 1 - i of one [P, T] score matrix (P <= T) keep
+// i + 1 and P - i columns, P + 1 together, so both kept parts fit one row-sized buffer.  They
+// are staged by two bulk copies (row A's vectors, then row B's) and each thread folds the
+// vectors it reads into the state of the row they belong to; the two (m, l) states are merged
+// over the CTA together; then both rows are written (0 past each row's limit).  Half the CTAs of
+// one row per CTA, each with twice the bytes in flight.
+template <typename Tin, typename Tout, int NT>
+__global__ void __launch_bounds__(NT)
+softmax_ex_pair_kernel(const Tin *__restrict__ x, Tout *z, long long rows, int T, long long xs, long long zs,
+                       float mult, long long period, int *status) {
+    constexpr int E = Vec<Tin>::E;
+    extern __shared__ __align__(16) uint8_t srow[];
+    __shared__ uint64_t bar;
+    __shared__ float sh[2][64];
+    const long long half = (period + 1) / 2;                  // CTAs per score matrix
+    const long long blk = blockIdx.x / half, i = blockIdx.x % half;
+    const long long ra = blk * period + i, rb = blk * period + (period - 1 - i);
+    if (ra >= rows) return;                                   // past a last, partial matrix (rb > ra)
+    const bool has_b = rb != ra && rb < rows;                 // the middle row of an odd P is alone
+    const int la = (int)min((long long)T, i + 1), lb = has_b ? (int)min((long long)T, period - i) : 0;
+    const int na = (la + E - 1) / E, nb = (lb + E - 1) / E;   // 16-byte vectors copied per row
+    const Tin *xa = x + ra * xs, *xb = x + rb * xs;
+    const uint32_t sbuf = ptx::smem_u32(srow);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::mbar_init_fence();
+        ptx::mbar_expect_tx(ptx::smem_u32(&bar), (uint32_t)(na + nb) * 16u);
+        ptx::bulk_load(sbuf, xa, (uint32_t)na * 16u, ptx::smem_u32(&bar));
+        if (nb > 0) ptx::bulk_load(sbuf + (uint32_t)na * 16u, xb, (uint32_t)nb * 16u, ptx::smem_u32(&bar));
+    }
+    __syncthreads();
+    const bool ok = ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr);
+    if (!__syncthreads_and(ok)) {
+        // the copies never completed: record it, give them a bounded chance to land, leave
+        if (threadIdx.x == 0) {
+            atomicExch(status, kStatusTimeout);
+            ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr, 20000000ull);
+        }
+        __syncthreads();
+        return;
+    }
+    const Tin *sx = reinterpret_cast<const Tin *>(srow);
+    float ma = -INFINITY, lA = 0.f, mb = -INFINITY, lB = 0.f;
+    for (int v = threadIdx.x; v < na + nb; v += NT) {
+        const bool in_b = v >= na;                            // row A or B
+        const int col0 = (v - (in_b ? na : 0)) * E, lim = in_b ? lb : la;
+        float f[E];
+        Vec<Tin>::load_shared(sx + v * E, f);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            f[e] = (col0 + e < lim) ? f[e] * mult : -INFINITY;
+            mx = fmaxf(mx, f[e]);
+        }
+        const float mo = in_b ? mb : ma, lo = in_b ? lB : lA;
+        const float mn = fmaxf(mo, mx);
+        const float mr = (mn == -INFINITY) ? 0.f : mn;
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) sum += ex2_approx(f[e] - mr);
+        const float ln = lo * ex2_approx(mo - mr) + sum;
+        if (in_b) {
+            mb = mn;
+            lB = ln;
+        } else {
+            ma = mn;
+            lA = ln;
+        }
+    }
+    cta_merge_ml(ma, lA, sh[0]);
+    cta_merge_ml(mb, lB, sh[1]);
+    const int nvec = T / E;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        if (w == 1 && !has_b) break;
+        const float mw = w ? mb : ma, lw = w ? lB : lA;
+        const float mref = (mw == -INFINITY) ? 0.f : mw;
+        const float inv = lw > 0.f ? 1.f / lw : 0.f;
+        const int n = w ? nb : na, lim = w ? lb : la;
+        const Tin *sw = sx + (w ? na : 0) * E;
+        Tout *zr = z + (w ? rb : ra) * zs;
+        for (int v = threadIdx.x; v < nvec; v += NT) {
+            float f[E];
+            if (v < n) {
+                Vec<Tin>::load_shared(sw + v * E, f);
+#pragma unroll
+                for (int e = 0; e < E; ++e) f[e] = (v * E + e < lim) ? ex2_approx(f[e] * mult - mref) * inv : 0.f;
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) f[e] = 0.f;
+            }
+            store_vec<E>(zr + (long long)v * E, f);
+        }
     }
 }
 
@@ -316,20 +436,34 @@ cudaError_t launch_typed(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
     const unsigned rows = (unsigned)q.rows;
     const bool aligned = q.T % E == 0 && al16(x, q.xs * (long long)sizeof(Tin)) &&
                          al16(z, q.zs * (long long)sizeof(Tout));
+    if (aligned && q.period > 0 && q.period <= q.T && (uint64_t)q.T * sizeof(Tin) <= 8 * 1024) {
+        // short causal rows: two complementary rows per CTA (buffer: P + 1 columns and the
+        // rounding of two rows to whole vectors)
+        const size_t smem = ((size_t)q.T / E + 2) * 16;
+        const long long half = (q.period + 1) / 2;
+        const long long ctas = (q.rows + q.period - 1) / q.period * half;
+        if (ctas < (1LL << 31)) {
+            softmax_ex_pair_kernel<Tin, Tout, 64><<<(unsigned)ctas, 64, smem, s>>>(x, z, q.rows, (int)q.T, q.xs, q.zs,
+                                                                                  q.mult, q.period, q.status);
+            count_launches(1);
+            return cudaGetLastError();
+        }
+    }
     if (aligned && (uint64_t)q.T * sizeof(Tin) <= kSmemRowBytes) {
-        const cudaError_t attr_err =
-            set_max_dynamic_smem((const void *)softmax_ex_smem_kernel<Tin, Tout, 256>, (int)kSmemRowBytes);
-        if (attr_err != cudaSuccess) return attr_err;
         const size_t smem = (size_t)q.T * sizeof(Tin);
-        if (smem <= 8 * 1024)
-            softmax_ex_smem_kernel<Tin, Tout, 64><<<rows, 64, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
-                                                                        q.period, q.status);
-        else if (smem <= 16 * 1024)
-            softmax_ex_smem_kernel<Tin, Tout, 128><<<rows, 128, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
-                                                                          q.period, q.status);
-        else
-            softmax_ex_smem_kernel<Tin, Tout, 256><<<rows, 256, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
-                                                                          q.period, q.status);
+        if (smem <= 8 * 1024) {
+            softmax_ex_smem_kernel<Tin, Tout, 64, 1><<<rows, 64, smem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
+                                                                                  q.period, q.status);
+        } else if (smem <= 16 * 1024) {
+            softmax_ex_smem_kernel<Tin, Tout, 128, 1><<<rows, 128, smem, s>>>(x, z, (int)q.T, q.xs, q.zs,
+                                                                                    q.mult, q.period, q.status);
+        } else {
+            const cudaError_t attr_err = set_max_dynamic_smem(
+                (const void *)softmax_ex_smem_kernel<Tin, Tout, 256, 2>, (int)kSmemRowBytes);
+            if (attr_err != cudaSuccess) return attr_err;
+            softmax_ex_smem_kernel<Tin, Tout, 256, 2><<<rows, 256, smem, s>>>(x, z, (int)q.T, q.xs, q.zs,
+                                                                                        q.mult, q.period, q.status);
+        }
         count_launches(1);
         return cudaGetLastError();
     }

@@ -80,6 +80,33 @@ def test_causal_periods_long_rows(osf, dtype, rows, T, period):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,T,period", [(1001, 1024, 333), (64, 512, 64), (7, 256, 8), (96, 128, 96)])
+def test_causal_row_pairs(osf, dtype, rows, T, period):
+    """Short causal rows (P <= T) run two complementary rows of a score matrix per CTA: an odd
+    period (the middle row alone), a last partial matrix (rows % P != 0, partners past the end),
+    fewer rows than one period, and in place."""
+    x32 = (si.normal_f32((rows, T), rows * 7 + T, si.STREAM_X) * 9).astype(np.float32)
+    x = to_dev(x32, dtype)
+    ref = oracle.softmax_masked(values(x), 0.7, period)
+    z = osf.osf_softmax_rows_ex(x, scale=0.7, causal_period=period)
+    check(z, ref, f"pairs {dtype} rows={rows} T={T} period={period}")
+    assert np.all(values(z)[ref == 0] == 0), "masked columns must be exactly zero"
+    w = osf.osf_softmax_rows_ex(x, x, scale=0.7, causal_period=period)   # in place
+    check(w, ref, f"pairs in place {dtype}")
+
+
+def test_causal_bf16_full_size(osf):
+    """The causal attention-weight workload (8 heads x [4096, 4096] bf16, scale 128^-0.5) as the
+    benchmark runs it: every row against the oracle, in blocks of rows."""
+    rows, T = 8 * 4096, 4096
+    x = torch.from_numpy(si.softmax_rows_input(rows, T, seed=0)).cuda().to(torch.bfloat16)
+    z = osf.osf_softmax_rows_ex(x, scale=128 ** -0.5, causal_period=4096)
+    for r0 in range(0, rows, 4096):
+        ref = oracle.softmax_masked(values(x[r0:r0 + 4096]), 128 ** -0.5, 4096)
+        check(z[r0:r0 + 4096], ref, f"causal bf16 8x4096x4096 head {r0 // 4096}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_padded_row_strides_and_in_place(osf, dtype):
     x32 = si.softmax_rows_input(40, 1000, seed=5)
     x = to_dev(x32, dtype, pad=24)          # row stride 1024: aligned
