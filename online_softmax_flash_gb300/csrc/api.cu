@@ -8,8 +8,8 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
-#include <set>
-#include <tuple>
+#include <map>
+#include <utility>
 
 #include "osf_internal.cuh"
 #include "softmax_ex.cuh"
@@ -25,15 +25,16 @@ void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::me
 
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes) {
     static std::mutex mu;
-    static std::set<std::tuple<int, const void *, int>> done;   // (device, kernel, bytes)
+    static std::map<std::pair<int, const void *>, int> done;   // (device, kernel) -> limit set
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_tuple(dev, kernel, bytes);
-    if (done.count(key)) return cudaSuccess;
+    const auto key = std::make_pair(dev, kernel);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;   // the limit is only raised
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.insert(key);
+    if (e == cudaSuccess) done[key] = bytes;
     return e;
 }
 

@@ -96,9 +96,10 @@ int device_sm_count(int *sms);
 
 // Count of kernels launched by the library (diagnostics; see osf_launch_count).
 void count_launches(int n);
-// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device.  The attribute
-// belongs to the device's context, so every device is configured on its first use there;
-// thread-safe, and a no-op once a device is configured.
+// Raise `kernel`'s dynamic shared-memory limit to at least `bytes` on the current device.  The
+// attribute belongs to the device's context, so every device is configured on its first use
+// there; the limit is only ever raised (a smaller request after a larger one keeps the larger
+// limit); thread-safe, and a no-op when the limit already suffices.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
 // Launch `kernel` as a programmatic dependent of the previous kernel in the stream: it is

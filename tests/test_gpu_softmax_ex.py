@@ -129,3 +129,12 @@ def test_bf16_rows_full_size(osf):
     z = osf.osf_softmax_rows_ex(x)
     for r0 in range(0, rows, 512):
         check(z[r0:r0 + 512], oracle.softmax_masked(values(x[r0:r0 + 512])), f"bf16 4096x32768 rows {r0}+")
+
+
+def test_long_rows_after_shorter_ones(osf):
+    """Row lengths whose shared-memory needs differ, in the order long, short, long: the kernels'
+    dynamic shared-memory limit is only ever raised, so the second long call still launches."""
+    for T in (32768, 16384, 32768):
+        x32 = si.softmax_rows_input(5, T, seed=T + 1)
+        x = to_dev(x32, torch.bfloat16)
+        check(osf.osf_softmax_rows_ex(x), oracle.softmax_masked(values(x)), f"bf16 T={T}")
