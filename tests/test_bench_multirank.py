@@ -70,3 +70,20 @@ def test_reference_arm_rank0_prints_one_line(capsys):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_compact_suite_entry_and_baseline_configs():
+    """The bench line's suite entries are short objects carrying the roofline; every problem
+    statement configuration is a workload of the bench, and one core of the oracle is a process
+    pinned to one CPU."""
+    sys.path.insert(0, ROOT)
+    import bench
+    e = {"value": 1.5, "unit": "GB/s", "ms_per_step": 0.2,
+         "roofline": {"bound": "hbm", "peak": 6769.4, "frac": 0.5, "traffic": 1e6}}
+    c = bench.compact(e, [0.1, 0.05])
+    assert c == {"v": 1.5, "u": "GB/s", "ms": 0.2, "rl": {"bound": "hbm", "peak": 6769.4, "frac": 0.5, "dram": 1e6},
+                 "oracle": [0.1, 0.05]}
+    assert "oracle" not in bench.compact(e)
+    assert set(bench.BASELINE_CONFIGS) <= set(bench.WORKLOADS)
+    one = bench.oracle_one_core("single_head_m64_n100", 0.2)
+    assert one is not None and one["cores"] == 1 and one["value"] > 0 and one["unit"] == "TFLOP/s"
