@@ -31,9 +31,11 @@ constexpr int kExChunkThreads = 512;
 template <typename T> struct Vec;
 template <> struct Vec<float> {
     static constexpr int E = 4;
-    __device__ __forceinline__ static void load_shared(const float *p, float (&f)[4]) {
-        const float4 a = *reinterpret_cast<const float4 *>(p);
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    static constexpr uint32_t SGN = 0x80000000u;   // the sign bit of each element of a 32-bit word
+    // 16 raw bytes to E floats, each with its sign flipped by `sgn` (0 or SGN)
+    __device__ __forceinline__ static void unpack(uint4 a, uint32_t sgn, float (&f)[4]) {
+        f[0] = __uint_as_float(a.x ^ sgn); f[1] = __uint_as_float(a.y ^ sgn);
+        f[2] = __uint_as_float(a.z ^ sgn); f[3] = __uint_as_float(a.w ^ sgn);
     }
     __device__ __forceinline__ static void load(const float *p, float (&f)[4]) {
         const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
@@ -42,9 +44,9 @@ template <> struct Vec<float> {
 };
 template <> struct Vec<__nv_bfloat16> {
     static constexpr int E = 8;
-    __device__ __forceinline__ static void load_shared(const __nv_bfloat16 *p, float (&f)[8]) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(p);
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    static constexpr uint32_t SGN = 0x80008000u;
+    __device__ __forceinline__ static void unpack(uint4 a, uint32_t sgn, float (&f)[8]) {
+        const uint32_t w[4] = {a.x ^ sgn, a.y ^ sgn, a.z ^ sgn, a.w ^ sgn};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             f[2 * i] = __uint_as_float(w[i] << 16);
@@ -109,6 +111,61 @@ __device__ __forceinline__ void cta_merge_ml(float &m, float &l, float *sh /* 2*
 
 __device__ __forceinline__ long long row_limit(long long row, long long T, long long period) {
     return period > 0 ? min(T, row % period + 1) : T;
+}
+
+// The staged kernels' arithmetic on one 16-byte vector of E values, columns [col0, col0 + E), in
+// base-2 units of x * a with a = |scale| * log2 e (a negative scale is applied by flipping the
+// values' signs on load).  Values are paired for f32x2 FMA / add / multiply; columns at or past
+// `lim` are dropped (-inf, then 0), and a vector wholly inside the limit takes no per-element test.
+template <int E>
+__device__ __forceinline__ void fold_vec(float (&f)[E], int col0, int lim, float a, float &m, float &l) {
+    if (col0 + E > lim) {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (col0 + e >= lim) f[e] = -INFINITY;
+    }
+    float mx = ptx::fmax3(f[0], f[1], f[2]);
+#pragma unroll
+    for (int e = 3; e + 1 < E; e += 2) mx = ptx::fmax3(mx, f[e], f[e + 1]);
+    if constexpr (E % 2 == 0) mx = fmaxf(mx, f[E - 1]);
+    const float mn = fmaxf(m, mx * a);
+    const float mr = (mn == -INFINITY) ? 0.f : mn;
+    const uint64_t a2 = ptx::f2_pack(a, a), n2 = ptx::f2_pack(-mr, -mr);
+    uint64_t acc = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+        float p0, p1;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(f[2 * k], f[2 * k + 1]), a2, n2), p0, p1);
+        acc = ptx::f2_add(acc, ptx::f2_pack(ex2_approx(p0), ex2_approx(p1)));
+    }
+    float lo, hi;
+    ptx::f2_unpack(acc, lo, hi);
+    l = l * ex2_approx(m - mr) + (lo + hi);
+    m = mn;
+}
+
+// z for one vector: 2^(x a - mref) / l for kept columns (`have`: the vector was loaded), else 0.
+template <int E, typename Tout>
+__device__ __forceinline__ void emit_vec(const float (&f)[E], int col0, int lim, bool have, float a, float mref,
+                                         float inv, Tout *dst) {
+    float o[E];
+    if (have && col0 + E <= lim) {
+        const uint64_t a2 = ptx::f2_pack(a, a), n2 = ptx::f2_pack(-mref, -mref), i2 = ptx::f2_pack(inv, inv);
+#pragma unroll
+        for (int k = 0; k < E / 2; ++k) {
+            float p0, p1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(f[2 * k], f[2 * k + 1]), a2, n2), p0, p1);
+            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(ex2_approx(p0), ex2_approx(p1)), i2), o[2 * k], o[2 * k + 1]);
+        }
+    } else if (!have || col0 >= lim) {
+        // past the row's limit: zeros, with no exponential evaluated
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = 0.f;
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = (col0 + e < lim) ? ex2_approx(f[e] * a - mref) * inv : 0.f;
+    }
+    store_vec<E>(dst, o);
 }
 
 // One CTA per row; thread t holds vectors t + k * blockDim (k < VPT) of the row in registers.
@@ -204,6 +261,8 @@ softmax_ex_smem_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, 
         }
     }
     const Tin *sx = reinterpret_cast<const Tin *>(srow);
+    const float a = fabsf(mult);
+    const uint32_t sgn = mult < 0.f ? Vec<Tin>::SGN : 0u;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
 #pragma unroll 1
@@ -214,20 +273,8 @@ softmax_ex_smem_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, 
         if (!ok) break;
         for (int i = v0 + threadIdx.x; i < v1; i += NT) {
             float f[E];
-            Vec<Tin>::load_shared(sx + i * E, f);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                f[e] = (i * E + e < lim) ? f[e] * mult : -INFINITY;
-                mx = fmaxf(mx, f[e]);
-            }
-            const float mn = fmaxf(m, mx);
-            const float mr = (mn == -INFINITY) ? 0.f : mn;
-            float s = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) s += ex2_approx(f[e] - mr);
-            l = l * ex2_approx(m - mr) + s;
-            m = mn;
+            Vec<Tin>::unpack(*reinterpret_cast<const uint4 *>(sx + i * E), sgn, f);
+            fold_vec<E>(f, i * E, lim, a, m, l);
         }
     }
     if (!__syncthreads_and(ok)) {
@@ -245,15 +292,92 @@ softmax_ex_smem_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, 
     const int nvec = T / E;
     for (int i = threadIdx.x; i < nvec; i += NT) {
         float f[E];
-        if (i < nload) {
-            Vec<Tin>::load_shared(sx + i * E, f);
-#pragma unroll
-            for (int e = 0; e < E; ++e) f[e] = (i * E + e < lim) ? ex2_approx(f[e] * mult - mref) * inv : 0.f;
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) f[e] = 0.f;
+        if (i < nload) Vec<Tin>::unpack(*reinterpret_cast<const uint4 *>(sx + i * E), sgn, f);
+        emit_vec<E, Tout>(f, i * E, lim, i < nload, a, mref, inv, zr + (long long)i * E);
+    }
+}
+
+// Rows of 32-64 KB, one CTA of NT threads per row: the first h vectors of the row are copied into
+// shared memory by one bulk copy, the rest are loaded into registers (VPT 16-byte vectors per
+// thread, kept packed), so a CTA needs half a row of shared memory and four rows are in flight
+// per SM instead of three.  (m, l) over the register half while the copy lands, then over the
+// shared half; z from both.
+template <typename Tin, typename Tout, int NT, int VPT>
+__global__ void __launch_bounds__(NT)
+softmax_ex_split_kernel(const Tin *__restrict__ x, Tout *z, int T, long long xs, long long zs, float mult,
+                        long long period, int *status) {
+    constexpr int E = Vec<Tin>::E;
+    extern __shared__ __align__(16) uint8_t srow[];
+    __shared__ uint64_t bar;
+    __shared__ float sh[64];
+    const long long row = blockIdx.x;
+    const Tin *xr = x + row * xs;
+    Tout *zr = z + row * zs;
+    const int lim = (int)row_limit(row, T, period);
+    const int nvec = T / E, h = nvec - VPT * NT;           // vectors [0, h) in shared memory
+    const int nload = (lim + E - 1) / E;                   // vectors that hold kept columns
+    const int ns = min(h, nload);                          // of them, copied
+    const uint32_t sbuf = ptx::smem_u32(srow);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::mbar_init_fence();
+        if (ns > 0) {
+            ptx::mbar_expect_tx(ptx::smem_u32(&bar), (uint32_t)ns * 16u);
+            ptx::bulk_load(sbuf, xr, (uint32_t)ns * 16u, ptx::smem_u32(&bar));
         }
-        store_vec<E>(zr + (long long)i * E, f);
+    }
+    // the register half: vector h + k * NT + threadIdx.x
+    uint4 rv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int i = h + k * NT + (int)threadIdx.x;
+        rv[k] = (i < nload) ? __ldcs(reinterpret_cast<const uint4 *>(xr + (long long)i * E)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    const float a = fabsf(mult);
+    const uint32_t sgn = mult < 0.f ? Vec<Tin>::SGN : 0u;
+    float m = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int i = h + k * NT + (int)threadIdx.x;
+        if (i < nload) {
+            float f[E];
+            Vec<Tin>::unpack(rv[k], sgn, f);
+            fold_vec<E>(f, i * E, lim, a, m, l);
+        }
+    }
+    const bool ok = ns <= 0 || ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr);
+    if (!__syncthreads_and(ok)) {
+        // the copy never completed: record it, give it a bounded chance to land, leave
+        if (threadIdx.x == 0) {
+            atomicExch(status, kStatusTimeout);
+            ptx::mbar_wait(ptx::smem_u32(&bar), 0, nullptr, 20000000ull);
+        }
+        __syncthreads();
+        return;
+    }
+    const Tin *sx = reinterpret_cast<const Tin *>(srow);
+    for (int i = threadIdx.x; i < ns; i += NT) {
+        float f[E];
+        Vec<Tin>::unpack(*reinterpret_cast<const uint4 *>(sx + i * E), sgn, f);
+        fold_vec<E>(f, i * E, lim, a, m, l);
+    }
+    cta_merge_ml(m, l, sh);
+    const float mref = (m == -INFINITY) ? 0.f : m;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    for (int i = threadIdx.x; i < h; i += NT) {
+        float f[E];
+        if (i < ns) Vec<Tin>::unpack(*reinterpret_cast<const uint4 *>(sx + i * E), sgn, f);
+        emit_vec<E, Tout>(f, i * E, lim, i < ns, a, mref, inv, zr + (long long)i * E);
+    }
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int i = h + k * NT + (int)threadIdx.x;
+        if (i < nvec) {
+            float f[E];
+            Vec<Tin>::unpack(rv[k], sgn, f);
+            emit_vec<E, Tout>(f, i * E, lim, i < nload, a, mref, inv, zr + (long long)i * E);
+        }
     }
 }
 
@@ -299,32 +423,15 @@ softmax_ex_pair_kernel(const Tin *__restrict__ x, Tout *z, long long rows, int T
         return;
     }
     const Tin *sx = reinterpret_cast<const Tin *>(srow);
+    const float a = fabsf(mult);
+    const uint32_t sgn = mult < 0.f ? Vec<Tin>::SGN : 0u;
     float ma = -INFINITY, lA = 0.f, mb = -INFINITY, lB = 0.f;
     for (int v = threadIdx.x; v < na + nb; v += NT) {
         const bool in_b = v >= na;                            // row A or B
-        const int col0 = (v - (in_b ? na : 0)) * E, lim = in_b ? lb : la;
         float f[E];
-        Vec<Tin>::load_shared(sx + v * E, f);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            f[e] = (col0 + e < lim) ? f[e] * mult : -INFINITY;
-            mx = fmaxf(mx, f[e]);
-        }
-        const float mo = in_b ? mb : ma, lo = in_b ? lB : lA;
-        const float mn = fmaxf(mo, mx);
-        const float mr = (mn == -INFINITY) ? 0.f : mn;
-        float sum = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) sum += ex2_approx(f[e] - mr);
-        const float ln = lo * ex2_approx(mo - mr) + sum;
-        if (in_b) {
-            mb = mn;
-            lB = ln;
-        } else {
-            ma = mn;
-            lA = ln;
-        }
+        Vec<Tin>::unpack(*reinterpret_cast<const uint4 *>(sx + v * E), sgn, f);
+        if (in_b) fold_vec<E>(f, (v - na) * E, lb, a, mb, lB);
+        else fold_vec<E>(f, v * E, la, a, ma, lA);
     }
     cta_merge_ml(ma, lA, sh[0]);
     cta_merge_ml(mb, lB, sh[1]);
@@ -340,15 +447,8 @@ softmax_ex_pair_kernel(const Tin *__restrict__ x, Tout *z, long long rows, int T
         Tout *zr = z + (w ? rb : ra) * zs;
         for (int v = threadIdx.x; v < nvec; v += NT) {
             float f[E];
-            if (v < n) {
-                Vec<Tin>::load_shared(sw + v * E, f);
-#pragma unroll
-                for (int e = 0; e < E; ++e) f[e] = (v * E + e < lim) ? ex2_approx(f[e] * mult - mref) * inv : 0.f;
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e) f[e] = 0.f;
-            }
-            store_vec<E>(zr + (long long)v * E, f);
+            if (v < n) Vec<Tin>::unpack(*reinterpret_cast<const uint4 *>(sw + v * E), sgn, f);
+            emit_vec<E, Tout>(f, v * E, lim, v < n, a, mref, inv, zr + (long long)v * E);
         }
     }
 }
@@ -457,6 +557,11 @@ cudaError_t launch_typed(const SoftmaxExProblem &q, float *ws, cudaStream_t s) {
         } else if (smem <= 16 * 1024) {
             softmax_ex_smem_kernel<Tin, Tout, 128, 1><<<rows, 128, smem, s>>>(x, z, (int)q.T, q.xs, q.zs,
                                                                                     q.mult, q.period, q.status);
+        } else if (q.T / E > 8 * 256 && q.T / E <= 2 * 8 * 256) {
+            // 32-64 KB rows: half in shared memory, 8 vectors per thread in registers
+            const size_t hsmem = (size_t)(q.T / E - 8 * 256) * 16;
+            softmax_ex_split_kernel<Tin, Tout, 256, 8><<<rows, 256, hsmem, s>>>(x, z, (int)q.T, q.xs, q.zs, q.mult,
+                                                                                 q.period, q.status);
         } else {
             const cudaError_t attr_err = set_max_dynamic_smem(
                 (const void *)softmax_ex_smem_kernel<Tin, Tout, 256, 2>, (int)kSmemRowBytes);

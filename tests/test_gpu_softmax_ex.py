@@ -138,3 +138,29 @@ def test_long_rows_after_shorter_ones(osf):
         x32 = si.softmax_rows_input(5, T, seed=T + 1)
         x = to_dev(x32, torch.bfloat16)
         check(osf.osf_softmax_rows_ex(x), oracle.softmax_masked(values(x)), f"bf16 T={T}")
+
+
+@pytest.mark.parametrize("dtype,T,rows,period", [(torch.bfloat16, 17000, 1000, 1000), (torch.bfloat16, 20000, 6, 0),
+                                                 (torch.float32, 16384, 9, 0), (torch.float32, 12000, 700, 700)])
+def test_rows_half_shared_half_registers(osf, dtype, T, rows, period):
+    """Rows of 32-64 KB keep their first part in shared memory and the rest in registers: causal
+    limits before, at and after the split column, and whole rows."""
+    x32 = (si.normal_f32((rows, T), rows + T, si.STREAM_X) * 7).astype(np.float32)
+    x = to_dev(x32, dtype)
+    z = osf.osf_softmax_rows_ex(x, scale=0.9, causal_period=period)
+    ref = oracle.softmax_masked(values(x), 0.9, period)
+    check(z, ref, f"split {dtype} T={T} rows={rows} period={period}")
+    if period:
+        assert np.all(values(z)[ref == 0] == 0), "masked columns must be exactly zero"
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,T,period", [(64, 2048, 64), (33, 1000, 0), (12, 6000, 0), (5, 12000, 0),
+                                           (4, 20000, 0), (3, 32768, 0)])
+def test_negative_scale(osf, dtype, rows, T, period):
+    """A negative scale is applied as |scale| to the values with their signs flipped on load; every
+    staged path (paired causal rows, one CTA of 64, 128 or 256 threads, half in registers)."""
+    x32 = (si.normal_f32((rows, T), rows * 3 + T, si.STREAM_X) * 5).astype(np.float32)
+    x = to_dev(x32, dtype)
+    z = osf.osf_softmax_rows_ex(x, scale=-0.6, causal_period=period)
+    check(z, oracle.softmax_masked(values(x), -0.6, period), f"negative scale {dtype} T={T} period={period}")
