@@ -273,6 +273,8 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &mq, const CUtenso
         const float lse2 = row_ok ? p.lse[grow] * kLog2e : INFINITY;
         const float dvr = row_ok ? p.dvec[grow] : 0.f;
         const float c2 = p.scale_log2;
+        // packed pairs: scale, -lse and -D of this row
+        const uint64_t c22 = f2_pack(c2, c2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-dvr, -dvr);
         const int col0 = h * 64;   // this warp's score columns
         bool ok = true;
         for (int j = 0; j < n; ++j) {
@@ -294,9 +296,12 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &mq, const CUtenso
                 tmem_ld32(tS + lane_off + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 64; ++k) {
-                    const float e = ex2_approx(fmaf(__uint_as_float(s[k]), c2, -lse2));
-                    pv[k] = (full || k < lim) ? e : 0.f;
+                for (int k = 0; k < 64; k += 2) {
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), c22, nl2), a0, a1);
+                    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                    pv[k] = (full || k < lim) ? e0 : 0.f;
+                    pv[k + 1] = (full || k + 1 < lim) ? e1 : 0.f;
                 }
             }
             tc_fence_before();
@@ -314,7 +319,10 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &mq, const CUtenso
                 tmem_ld_wait();
                 float ds[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) ds[k] = pv[32 * c + k] * (__uint_as_float(d[k]) - dvr);
+                for (int k = 0; k < 32; k += 2)
+                    f2_unpack(f2_mul(f2_pack(pv[32 * c + k], pv[32 * c + k + 1]),
+                                     f2_add(f2_pack(__uint_as_float(d[k]), __uint_as_float(d[k + 1])), nd2)),
+                              ds[k], ds[k + 1]);
                 pack_store16(tdS + lane_off + h * 32 + 16 * c, ds);
             }
             tmem_st_wait();
@@ -463,8 +471,9 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
 #pragma unroll
             for (int i = 0; i < TB / 32; ++i) {
                 const int c = lane + 32 * i, q = qt * TB + c;
-                tl[c] = q < p.Sq ? p.lse[row0 + q] * kLog2e : INFINITY;
-                td[c] = q < p.Sq ? p.dvec[row0 + q] : 0.f;
+                // negated, the addends of the compute warps' packed FMA and add
+                tl[c] = q < p.Sq ? -p.lse[row0 + q] * kLog2e : -INFINITY;
+                td[c] = q < p.Sq ? -p.dvec[row0 + q] : 0.f;
             }
             mbar_arrive(smem_u32(&bars.t_full[st]));
         }
@@ -474,7 +483,7 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
         const int q4 = warp & 3, h = (warp - 4) >> 2;
         const int r = q4 * 32 + lane, key = key0 + r;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const float c2 = p.scale_log2;
+        const uint64_t c22 = f2_pack(p.scale_log2, p.scale_log2);
         const int col0 = h * 64;   // this warp's query columns
         bool ok = true;
         for (int j = 0; j < n; ++j) {
@@ -501,13 +510,17 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
                 tmem_ld_wait();
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 l = tl4[8 * c + k4];
-                    const float lv[4] = {l.x, l.y, l.z, l.w};
+                    const float4 l = tl4[8 * c + k4];   // -lse (base 2) of four query columns
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 4; e += 2) {
                         const int k = 4 * k4 + e;
-                        const float x = ex2_approx(fmaf(__uint_as_float(s[k]), c2, -lv[e]));
-                        pv[32 * c + k] = (full || 32 * c + k >= qmin) ? x : 0.f;
+                        float a0, a1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), c22,
+                                         e ? f2_pack(l.z, l.w) : f2_pack(l.x, l.y)),
+                                  a0, a1);
+                        const float x0 = ex2_approx(a0), x1 = ex2_approx(a1);
+                        pv[32 * c + k] = (full || 32 * c + k >= qmin) ? x0 : 0.f;
+                        pv[32 * c + k + 1] = (full || 32 * c + k + 1 >= qmin) ? x1 : 0.f;
                     }
                 }
                 pack_store16(tS + lane_off + col0 + 16 * c, *reinterpret_cast<const float(*)[32]>(pv + 32 * c));
@@ -529,12 +542,14 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
                 float ds[32];
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 dd = td4[8 * c + k4];
-                    const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+                    const float4 dd = td4[8 * c + k4];   // -D of four query columns
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 4; e += 2) {
                         const int k = 4 * k4 + e;
-                        ds[k] = pv[32 * c + k] * (__uint_as_float(d[k]) - dv[e]);
+                        f2_unpack(f2_mul(f2_pack(pv[32 * c + k], pv[32 * c + k + 1]),
+                                         f2_add(f2_pack(__uint_as_float(d[k]), __uint_as_float(d[k + 1])),
+                                                e ? f2_pack(dd.z, dd.w) : f2_pack(dd.x, dd.y))),
+                                  ds[k], ds[k + 1]);
                     }
                 }
                 pack_store16(tP + lane_off + col0 + 16 * c, ds);
