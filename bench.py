@@ -110,12 +110,12 @@ TRAFFIC = {
                      "bytes": 1012.50e6, "scope": "softmax_rows_resident_kernel<8>, one launch"},
     "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
                    "bytes": 756.78e6, "scope": "step: chunk state + chunk normalise kernels"},
-    "softmax_rows_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "574466ad3f2ec8ec",
-                          "bytes": 475.95e6, "scope": "softmax_ex_smem_kernel<bf16, bf16, 256, 2>, one launch"},
-    "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "574466ad3f2ec8ec",
-                            "bytes": 342.70e6, "scope": "softmax_ex_pair_kernel<bf16, bf16, 64>, one launch"},
-    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "0c7cd58496abe167",
-                            "bytes": 521.73e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
+    "softmax_rows_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "322a54acaf8bf1f2",
+                          "bytes": 475.60e6, "scope": "softmax_ex_split_kernel<bf16, bf16, 256, 8>, one launch"},
+    "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "322a54acaf8bf1f2",
+                            "bytes": 343.11e6, "scope": "softmax_ex_pair_kernel<bf16, bf16, 64>, one launch"},
+    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "217705f65f3906d7",
+                            "bytes": 523.54e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
     "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
                              "bytes": 4.34e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
     "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
@@ -324,60 +324,78 @@ _REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 
                 "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
 
+# Child process that reads NVML every millisecond and prints "monotonic_time sm_mhz max_mhz reasons
+# mem_mhz" lines (read-only queries); a separate process, so the sampling does not wait on this
+# process's interpreter lock while it launches work.
+_NVML_CHILD = r"""
+import ctypes, sys, time
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+assert lib.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+assert lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(sys.argv[1])), ctypes.byref(h)) == 0
+rf = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+sm, mx, rs, mem = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+print("ready", flush=True)
+while True:
+    lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm))
+    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+    rf(h, ctypes.byref(rs))
+    lib.nvmlDeviceGetClockInfo(h, 2, ctypes.byref(mem))
+    print(time.monotonic(), sm.value, mx.value, rs.value, mem.value, flush=True)
+    time.sleep(0.001)
+"""
+
+
 class NvmlSampler:
-    """SM clock, its maximum and the clock event reasons, read through NVML (read-only queries)
-    every ~1 ms by a thread while `open` is set; only samples taken inside that window count."""
+    """SM clock, its maximum, the clock event reasons and the memory clock, read through NVML about
+    every millisecond by a child process; only samples taken inside the window (first warm-up
+    step to last timed step, on the system's monotonic clock) count."""
 
     def __init__(self, index):
-        import ctypes
-        self.ct = ctypes
-        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
-        if self.lib.nvmlInit_v2() != 0:
-            raise OSError("nvmlInit failed")
-        self.h = ctypes.c_void_p()
-        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(_physical_index(index)), ctypes.byref(self.h)) != 0:
-            raise OSError("no NVML handle")
-        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        self.samples = []
-        self.open = False
-        self.stop_flag = False
-        self.thread = None
-
-    def _sample(self):
-        ct = self.ct
-        sm, mx, rs, mem = ct.c_uint(), ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
-        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(sm)) != 0:   # NVML_CLOCK_SM
-            return None
-        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
-        self.reasons_fn(self.h, ct.byref(rs))
-        self.lib.nvmlDeviceGetClockInfo(self.h, 2, ct.byref(mem))           # NVML_CLOCK_MEM
-        return float(sm.value), float(mx.value), int(rs.value), float(mem.value)
+        ctypes = __import__("ctypes")
+        ctypes.CDLL("libnvidia-ml.so.1")   # raises OSError where NVML is absent
+        self.index = _physical_index(index)
+        self.rows = []
+        self.windows = []
+        self.proc = None
 
     def start(self):
-        def run():
-            while not self.stop_flag:
-                if self.open:
-                    v = self._sample()
-                    if v and self.open:
-                        self.samples.append(v)
-                time.sleep(0.001)
-        self.thread = threading.Thread(target=run, daemon=True)
-        self.thread.start()
+        self.proc = subprocess.Popen([sys.executable, "-c", _NVML_CHILD, str(self.index)], stdout=subprocess.PIPE,
+                                     stderr=subprocess.DEVNULL, text=True)
+        if self.proc.stdout.readline().strip() != "ready":
+            raise OSError("NVML sampler did not start")
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = line.split()
+            if len(f) == 5:
+                self.rows.append((float(f[0]), float(f[1]), float(f[2]), int(f[3]), float(f[4])))
+
+    def window_open(self):
+        self.windows.append([time.monotonic(), None])
+
+    def window_close(self):
+        self.windows[-1][1] = time.monotonic()
 
     def stop(self):
-        self.stop_flag = True
-        if self.thread:
-            self.thread.join(timeout=2)
+        time.sleep(0.01)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
 
     def summary(self):
-        if not self.samples:
+        smp = [r[1:] for r in self.rows if any(a <= r[0] <= (b or a) for a, b in self.windows)]
+        if not smp:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
-        reasons = sorted(n for n, b in _REASON_BITS.items() if any(s[2] & b for s in self.samples))
-        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": max(s[1] for s in self.samples),
-                "reasons": reasons, "samples": len(self.samples), "window": "warm-up + timed steps",
-                "mem_mhz": [min(s[3] for s in self.samples), statistics.median(s[3] for s in self.samples)],
-                "source": "nvml, ~1 ms"}
+        reasons = sorted(n for n, b in _REASON_BITS.items() if any(s[2] & b for s in smp))
+        return {"sm_mhz": statistics.median(s[0] for s in smp), "sm_max_mhz": max(s[1] for s in smp),
+                "reasons": reasons, "samples": len(smp), "window": "warm-up + timed steps",
+                "mem_mhz": [min(s[3] for s in smp), statistics.median(s[3] for s in smp)],
+                "source": "nvml, ~1 ms, child process"}
 
 
 class ClockSampler:
@@ -409,6 +427,12 @@ class ClockSampler:
             if self.open:
                 self.samples.append([c.strip() for c in line.split(",")])
 
+    def window_open(self):
+        self.open = True
+
+    def window_close(self):
+        self.open = False
+
     def stop(self):
         if self.proc:
             self.proc.terminate()
@@ -429,11 +453,30 @@ class ClockSampler:
                 "source": "nvidia-smi, 50 ms"}
 
 
+class _Samplers:
+    """The NVML sampler, else the nvidia-smi one when NVML cannot be loaded or started."""
+
+    def __init__(self, index):
+        self.index = index
+        try:
+            self.s = NvmlSampler(index)
+        except (OSError, AttributeError):
+            self.s = ClockSampler(index)
+
+    def start(self):
+        try:
+            self.s.start()
+        except OSError:
+            self.s.stop()
+            self.s = ClockSampler(self.index)
+            self.s.start()
+
+    def __getattr__(self, name):
+        return getattr(self.s, name)
+
+
 def make_sampler(index):
-    try:
-        return NvmlSampler(index)
-    except (OSError, AttributeError):
-        return ClockSampler(index)
+    return _Samplers(index)
 
 
 # ----------------------------------------------------------------------------- timing
@@ -456,7 +499,7 @@ def time_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
     """Per-step CUDA-event times (ms) of ``fn`` on ``stream``, L2 flushed between steps."""
     import torch
     if sampler:
-        sampler.open = True
+        sampler.window_open()
     for _ in range(warmup):
         fn()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -475,7 +518,7 @@ def time_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     if sampler:
-        sampler.open = False
+        sampler.window_close()
     if barrier:
         barrier()
     torch.cuda.synchronize()
