@@ -336,13 +336,16 @@ assert lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(sys.argv[1])), ctypes
 rf = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
 sm, mx, rs, mem = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
 print("ready", flush=True)
+i = 0
 while True:
     lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm))
-    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
     rf(h, ctypes.byref(rs))
-    lib.nvmlDeviceGetClockInfo(h, 2, ctypes.byref(mem))
+    if i % 8 == 0:   # the maximum and the memory clock change rarely: every eighth sample
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        lib.nvmlDeviceGetClockInfo(h, 2, ctypes.byref(mem))
     print(time.monotonic(), sm.value, mx.value, rs.value, mem.value, flush=True)
-    time.sleep(0.001)
+    i += 1
+    time.sleep(0.0005)
 """
 
 
