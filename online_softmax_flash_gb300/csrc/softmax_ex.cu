@@ -119,15 +119,17 @@ __device__ __forceinline__ long long row_limit(long long row, long long T, long 
 // `lim` are dropped (-inf, then 0), and a vector wholly inside the limit takes no per-element test.
 template <int E>
 __device__ __forceinline__ void fold_vec(float (&f)[E], int col0, int lim, float a, float &m, float &l) {
+    static_assert(E == 4 || E == 8, "16-byte vectors of float32 or bfloat16");
     if (col0 + E > lim) {
 #pragma unroll
         for (int e = 0; e < E; ++e)
             if (col0 + e >= lim) f[e] = -INFINITY;
     }
+    // max of E values: 3-input max over f[0..2], then pairs f[3..4], f[5..6], then f[E - 1]
     float mx = ptx::fmax3(f[0], f[1], f[2]);
 #pragma unroll
     for (int e = 3; e + 1 < E; e += 2) mx = ptx::fmax3(mx, f[e], f[e + 1]);
-    if constexpr (E % 2 == 0) mx = fmaxf(mx, f[E - 1]);
+    mx = fmaxf(mx, f[E - 1]);
     const float mn = fmaxf(m, mx * a);
     const float mr = (mn == -INFINITY) ? 0.f : mn;
     const uint64_t a2 = ptx::f2_pack(a, a), n2 = ptx::f2_pack(-mr, -mr);
