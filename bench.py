@@ -110,10 +110,10 @@ TRAFFIC = {
                      "bytes": 1012.50e6, "scope": "softmax_rows_resident_kernel<8>, one launch"},
     "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
                    "bytes": 756.78e6, "scope": "step: chunk state + chunk normalise kernels"},
-    "softmax_rows_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "322a54acaf8bf1f2",
-                          "bytes": 475.60e6, "scope": "softmax_ex_split_kernel<bf16, bf16, 256, 8>, one launch"},
-    "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "322a54acaf8bf1f2",
-                            "bytes": 343.11e6, "scope": "softmax_ex_pair_kernel<bf16, bf16, 64>, one launch"},
+    "softmax_rows_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "d07ea9a9b6620ae0",
+                          "bytes": 475.47e6, "scope": "softmax_ex_split_kernel<bf16, bf16, 256, 8>, one launch"},
+    "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "d07ea9a9b6620ae0",
+                            "bytes": 343.07e6, "scope": "softmax_ex_pair_kernel<bf16, bf16, 64>, one launch"},
     "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "217705f65f3906d7",
                             "bytes": 523.54e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
     "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",

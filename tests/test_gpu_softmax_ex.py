@@ -164,3 +164,20 @@ def test_negative_scale(osf, dtype, rows, T, period):
     x = to_dev(x32, dtype)
     z = osf.osf_softmax_rows_ex(x, scale=-0.6, causal_period=period)
     check(z, oracle.softmax_masked(values(x), -0.6, period), f"negative scale {dtype} T={T} period={period}")
+
+
+@pytest.mark.parametrize("dtype,T", [(torch.bfloat16, 32768), (torch.float32, 16384), (torch.bfloat16, 4096)])
+def test_long_rows_strided_and_in_place(osf, dtype, T):
+    """Rows with a padded row stride (x and z strides differ) and in place, on the half-register
+    path (32-64 KB rows) and on the paired causal path."""
+    rows = 6
+    x32 = (si.normal_f32((rows, T), T + 11, si.STREAM_X) * 6).astype(np.float32)
+    x = to_dev(x32, dtype, pad=64)                        # row stride T + 64
+    period = rows if T == 4096 else 0
+    ref = oracle.softmax_masked(values(x), 1.3, period)
+    zbuf = torch.full((rows, T + 128), 5.0, dtype=dtype, device="cuda")
+    z = osf.osf_softmax_rows_ex(x, zbuf[:, :T], scale=1.3, causal_period=period)
+    check(z, ref, f"strided {dtype} T={T}")
+    assert torch.all(zbuf[:, T:] == 5.0), "padding of z written"
+    w = osf.osf_softmax_rows_ex(x, x, scale=1.3, causal_period=period)   # in place
+    check(w, ref, f"in place {dtype} T={T}")
