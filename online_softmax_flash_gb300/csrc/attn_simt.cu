@@ -209,6 +209,142 @@ attn_simt_kernel(const AttnProblem p) {
     }
 }
 
+// ---------------------------------------------------------------- few rows, few keys
+// float32 problems with few query rows and at most kRowsSk keys per head, D <= 64 (the M = 64,
+// N = 100, d = 32 `solve` of "softmax_attention", section "实现思路", is one): a CTA of kRowsW
+// warps owns kRowsW consecutive query rows of one (b, q head), one row per warp, as the page runs
+// one program per query.  The CTA first copies its kv head's whole K and V into shared memory
+// with asynchronous copies that are all issued before the first is waited for, so the kernel
+// pays one memory round trip instead of one per key block; each warp then runs the recurrence
+// over blocks of 64 keys, lane j scoring keys j and j + 32 of the block.
+constexpr int kRowsSk = 256;   // keys a CTA stages (K and V of one kv head)
+constexpr int kRowsW = 4;      // warps (query rows) per CTA
+
+template <int DP>
+struct RowsCfg {
+    static constexpr int KS = DP + 4;   // K row stride in floats: 16-byte aligned, and the 16-byte
+                                        // reads of eight consecutive keys hit distinct banks
+    static size_t smem_bytes(int sk_pad) { return (size_t)sk_pad * (KS + DP) * sizeof(float); }
+};
+
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// vec: K and V rows start on 16-byte boundaries and D % 4 == 0 (16-byte copies).
+template <int DP>
+__global__ void __launch_bounds__(kRowsW * 32) attn_rows_kernel(const AttnProblem p, int sk_pad, bool vec) {
+    using C = RowsCfg<DP>;
+    extern __shared__ __align__(16) float smem[];
+    float *Ks = smem;                   // [sk_pad][KS]
+    float *Vs = Ks + sk_pad * C::KS;    // [sk_pad][DP]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.y, b = bh / p.Hq, hq = bh % p.Hq;
+    const int kvh = hq / (p.Hq / p.Hkv);
+    const int D = p.D, Sk = p.Sk;
+    const float *Kg = static_cast<const float *>(p.k) + k_at(p, b, kvh, 0);
+    const float *Vg = static_cast<const float *>(p.v) + v_at(p, b, kvh, 0);
+
+    // K and V into shared memory; columns past D and keys past Sk are zeros
+    if (vec) {
+        const int per_row = D >> 2;
+        for (int idx = tid; idx < Sk * per_row; idx += kRowsW * 32) {
+            const int key = idx / per_row, c = (idx - key * per_row) * 4;
+            cp_async16(Ks + key * C::KS + c, Kg + (long long)key * p.k_ss + c);
+            cp_async16(Vs + key * DP + c, Vg + (long long)key * p.v_ss + c);
+        }
+    } else {
+        for (int idx = tid; idx < Sk * D; idx += kRowsW * 32) {
+            const int key = idx / D, c = idx - key * D;
+            cp_async4(Ks + key * C::KS + c, Kg + (long long)key * p.k_ss + c);
+            cp_async4(Vs + key * DP + c, Vg + (long long)key * p.v_ss + c);
+        }
+    }
+    for (int idx = tid; idx < sk_pad * DP; idx += kRowsW * 32) {
+        const int key = idx / DP, c = idx - key * DP;
+        if (key >= Sk || c >= D) {
+            Ks[key * C::KS + c] = 0.f;
+            Vs[key * DP + c] = 0.f;
+        }
+    }
+    // this warp's query row, in registers (the same addresses in every lane), loaded while the
+    // copies are in flight
+    const int row = blockIdx.x * kRowsW + warp;
+    const bool have_row = row < p.Sq;
+    float q[DP];
+    if (have_row) {
+        const float *Qg = static_cast<const float *>(p.q) + q_at(p, b, hq, row);
+#pragma unroll
+        for (int d = 0; d < DP; ++d) q[d] = d < D ? Qg[d] : 0.f;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (!have_row) return;
+
+    // keys this row sees: [0, lim)
+    int lim = Sk;
+    if (p.causal) lim = max(0, min(lim, row + p.causal_off + 1));
+    float m = -INFINITY, l = 0.f, acc[DP / 32];
+#pragma unroll
+    for (int c = 0; c < DP / 32; ++c) acc[c] = 0.f;
+    for (int kb = 0; kb < lim; kb += 64) {
+        float s[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int key = kb + 32 * h + lane;   // < sk_pad: staged (zeros past Sk)
+            const float *kr = Ks + key * C::KS;
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < DP; c += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(kr + c);
+                part[0] = fmaf(q[c], k4.x, part[0]);
+                part[1] = fmaf(q[c + 1], k4.y, part[1]);
+                part[2] = fmaf(q[c + 2], k4.z, part[2]);
+                part[3] = fmaf(q[c + 3], k4.w, part[3]);
+            }
+            const float dot = (part[0] + part[1]) + (part[2] + part[3]);
+            s[h] = key < lim ? dot * p.scale_log2 : -INFINITY;   // base 2, scale folded in
+        }
+        float bmax = fmaxf(s[0], s[1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+        const float m_new = fmaxf(m, bmax);   // finite: key kb < lim is in the block
+        const float alpha = ex2_approx(m - m_new);   // 0 on the first block (m = -inf)
+        const float p0 = ex2_approx(s[0] - m_new), p1 = ex2_approx(s[1] - m_new);
+        float rs = p0 + p1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+        l = l * alpha + rs;
+        m = m_new;
+#pragma unroll
+        for (int c = 0; c < DP / 32; ++c) acc[c] *= alpha;
+        // acc[c] (column lane + 32c) += sum over the block's keys of p_key * V[key][column]
+        const float *v0 = Vs + kb * DP + lane;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const float pa = __shfl_sync(0xffffffffu, p0, j), pb = __shfl_sync(0xffffffffu, p1, j);
+#pragma unroll
+            for (int c = 0; c < DP / 32; ++c)
+                acc[c] = fmaf(pb, v0[(32 + j) * DP + 32 * c], fmaf(pa, v0[j * DP + 32 * c], acc[c]));
+        }
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float *Og = static_cast<float *>(p.o) + o_at(p, b, hq, row);
+#pragma unroll
+    for (int c = 0; c < DP / 32; ++c)
+        if (lane + 32 * c < D) Og[lane + 32 * c] = acc[c] * inv;
+    if (p.lse && lane == 0)
+        p.lse[(long long)bh * p.Sq + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+}
+
 // Log-sum-exp combine of split partial states: M = max_s m_s, w_s = 2^(m_s - M),
 // O = sum_s w_s acc_s / sum_s w_s l_s, lse = (M + log2 L) ln 2.  One thread per four columns of
 // an output row.  The splits are taken eight at a time with every load of a group issued
@@ -297,9 +433,31 @@ cudaError_t launch_dp(const AttnProblem &p, cudaStream_t s) {
 
 int block_m(int D) { return D <= 128 ? 64 : 32; }
 
+// Problems the few-rows kernel runs: float32, D <= 64, at most kRowsSk keys, at most 2048 query
+// rows in all (512 CTAs, each staging its kv head's K and V).
+bool rows_eligible(const AttnProblem &p) {
+    return p.dtype == OSF_F32 && p.D <= 64 && p.Sk <= kRowsSk && (long long)p.B * p.Hq * p.Sq <= 2048;
+}
+
+template <int DP>
+cudaError_t launch_rows_t(const AttnProblem &p, cudaStream_t s) {
+    const int sk_pad = (p.Sk + 63) / 64 * 64;
+    const size_t smem = RowsCfg<DP>::smem_bytes(sk_pad);
+    const cudaError_t e = set_max_dynamic_smem((const void *)attn_rows_kernel<DP>, (int)RowsCfg<DP>::smem_bytes(kRowsSk));
+    if (e != cudaSuccess) return e;
+    // 16-byte copies when every K and V row starts on a 16-byte boundary
+    const bool vec = p.D % 4 == 0 && ((reinterpret_cast<uintptr_t>(p.k) | reinterpret_cast<uintptr_t>(p.v)) & 15) == 0 &&
+                     ((p.k_ss | p.k_sh | p.k_sb | p.v_ss | p.v_sh | p.v_sb) & 3) == 0;
+    const dim3 grid((unsigned)((p.Sq + kRowsW - 1) / kRowsW), (unsigned)(p.B * p.Hq));
+    attn_rows_kernel<DP><<<grid, kRowsW * 32, smem, s>>>(p, sk_pad, vec);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int attn_simt_pick_splits(const AttnProblem &p, int sm_count) {
+    if (rows_eligible(p)) return 1;
     const int BM = block_m(p.D);
     const long long ctas = (long long)((p.Sq + BM - 1) / BM) * p.B * p.Hq;
     const int n_kt = (p.Sk + BN - 1) / BN;
@@ -316,6 +474,7 @@ size_t attn_simt_partial_floats(int splits, long long rows, int D) {
 }
 
 cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t s) {
+    if (p.splits == 1 && rows_eligible(p)) return p.D <= 32 ? launch_rows_t<32>(p, s) : launch_rows_t<64>(p, s);
     return p.dtype == OSF_F32 ? launch_dp<float>(p, s) : launch_dp<__nv_bfloat16>(p, s);
 }
 
