@@ -237,3 +237,20 @@ def test_extreme_scores_stay_finite(osf):
         o = osf.osf_attn_fwd_gqa(dev(qq, dtype), dev(kk, dtype), dev(vv, dtype), causal=True)
         ref, _ = oracle.attention_gqa(f64(qq, dtype), f64(kk, dtype), f64(vv, dtype), causal=True)
         check(o, ref, dtype, f"extreme {dtype}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_on_every_key_tile(osf, D, causal):
+    """Keys scaled up along the sequence (key s by 1 + s/64), so a row's maximum grows by more
+    than the lazy-rescale threshold on almost every key tile: O is rescaled between P V
+    products on persistent multi-item CTAs (320 items, 8 key tiles each), where at D = 64 a
+    tile's earlier P V may still be queued behind later score products."""
+    B, Hq, Hkv, S = 2, 40, 8, 1024
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=D + causal)
+    k = (k * (1.0 + np.arange(S, dtype=np.float32) / 64.0)[None, None, :, None]).astype(np.float32)
+    qq, kk, vv = (si.f32_to_bf16_bits(a) for a in (q, k, v))
+    o = osf.osf_attn_fwd_gqa(dev(qq, "bf16"), dev(kk, "bf16"), dev(vv, "bf16"), causal=causal)
+    ref, _ = oracle.attention_gqa(f64(qq, "bf16"), f64(kk, "bf16"), f64(vv, "bf16"), causal=causal)
+    check(o, ref, "bf16", f"rescale every tile D={D} causal={causal}")
+    assert osf.osf_device_status() == osf.OSF_OK
