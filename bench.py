@@ -713,15 +713,35 @@ BASELINE_CONFIGS = ("single_head_m64_n100", "single_head_4096_f32", "single_head
 
 
 def compact(entry, oracle=None):
-    """A suite entry as a short object: value, unit, ms per step, and the roofline (bound, peak,
-    achieved fraction of it, DRAM bytes per launch from ncu or null); `oracle`: the oracle's
-    throughput in the same unit, [on all host cores, on one core]."""
+    """A suite entry as a short object: value, unit, ms per step (4 significant digits), and the
+    roofline: its bound, peak and the achieved fraction of it, and the DRAM megabytes per launch
+    from ncu (null when not captured for the current source); `oracle`: the oracle's throughput
+    in the same unit, [on all host cores, on one core]."""
     rl = entry["roofline"]
-    out = {"v": entry["value"], "u": entry["unit"], "ms": entry["ms_per_step"],
-           "rl": {"bound": rl["bound"], "peak": rl["peak"], "frac": rl["frac"], "dram": rl["traffic"]}}
+    g4 = lambda x: None if x is None else float(f"{x:.4g}")
+    out = {"v": g4(entry["value"]), "u": entry["unit"], "ms": g4(entry["ms_per_step"]), "bound": rl["bound"],
+           "peak": rl["peak"], "frac": rl["frac"], "dram_mb": None if rl["traffic"] is None else g4(rl["traffic"] / 1e6)}
     if oracle:
         out["oracle"] = oracle
     return out
+
+
+# Order of the suite in the result line: the configurations the metric is quoted on, and the
+# backward, come last, where a reader of only the end of the output still finds them.
+TAIL_FIRST = ("gqa_causal_backward",)
+
+
+def suite_order(names):
+    late = [n for n in TAIL_FIRST if n in names] + [n for n in BASELINE_CONFIGS if n in names]
+    return [n for n in names if n not in late] + late
+
+
+def headline_oracle(cpu):
+    """[all host cores, one core] oracle throughput of the headline workload, or None."""
+    if not cpu:
+        return None
+    one = cpu.get("one_core")
+    return [float(f"{cpu['value']:.4g}"), float(f"{one['value']:.4g}") if one else None]
 
 
 # ------------------------------------------------------------------------------ main
@@ -891,7 +911,10 @@ def main():
             "gpu_launches": res["launches"], "launches_per_step": res["launches_per_call"],
             "device_status": res["status"], "clocks": sampler.summary(),
             # last, and short, so that the end of the line holds every workload's number
-            "suite": {n: compact(e, suite_oracle.get(n)) for n, e in suite.items()},
+            "suite": {n: compact(suite[n], suite_oracle.get(n)) for n in suite_order(list(suite))},
+            # the headline again in the suite's short form, at the very end
+            "headline": {args.workload: compact({"value": value, "unit": res["unit"], "ms_per_step": mean_ms,
+                                                 "roofline": rl}, headline_oracle(cpu))},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

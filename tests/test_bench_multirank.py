@@ -81,9 +81,15 @@ def test_compact_suite_entry_and_baseline_configs():
     e = {"value": 1.5, "unit": "GB/s", "ms_per_step": 0.2,
          "roofline": {"bound": "hbm", "peak": 6769.4, "frac": 0.5, "traffic": 1e6}}
     c = bench.compact(e, [0.1, 0.05])
-    assert c == {"v": 1.5, "u": "GB/s", "ms": 0.2, "rl": {"bound": "hbm", "peak": 6769.4, "frac": 0.5, "dram": 1e6},
+    assert c == {"v": 1.5, "u": "GB/s", "ms": 0.2, "bound": "hbm", "peak": 6769.4, "frac": 0.5, "dram_mb": 1.0,
                  "oracle": [0.1, 0.05]}
     assert "oracle" not in bench.compact(e)
+    assert bench.compact({**e, "value": 1234.5678, "roofline": {**e["roofline"], "traffic": None}})["v"] == 1235.0
+    # the problem statement's configurations and the backward come last in the line
+    names = ["softmax_rows", "gqa_causal_prefill_bshd", "gqa_causal_backward", "single_head_m64_n100", "x"]
+    order = bench.suite_order(names)
+    assert order[:2] == ["gqa_causal_prefill_bshd", "x"] and order[2] == "gqa_causal_backward"
+    assert set(order[3:]) == {"softmax_rows", "single_head_m64_n100"}
     assert set(bench.BASELINE_CONFIGS) <= set(bench.WORKLOADS)
     one = bench.oracle_one_core("single_head_m64_n100", 0.2)
     assert one is not None and one["cores"] == 1 and one["value"] > 0 and one["unit"] == "TFLOP/s"
