@@ -67,8 +67,8 @@ constexpr int kMaxStages = 12;
 //   S = Qh Kh^T + Qh Km^T + Qm Kh^T + Qh Kl^T + Ql Kh^T + Qm Km^T
 // drops only terms of about 2^-24 relative: the exponent turns an absolute error of S into a
 // relative error of P, so S must be as good as float32.  V and P (in [0, 1]) have two parts,
-// h and l = bf16(x - h) (about 2^-17 relative), and O += Ph [Vh | Vl] + Pl Vh, with
-// O = O[:, :D] + O[:, D:] at the end.
+// h and l = bf16(x - h) (about 2^-17 relative), and O += Ph [Vh | Vl] + Pl [Vh | Vl] (Pl Vh alone
+// when Vh and Vl are not in adjacent ring stages), with O = O[:, :D] + O[:, D:] at the end.
 template <int D, bool X3>
 struct TcCfg {
     static constexpr uint32_t TILE = BN * D * 2;                 // one [128 x D] bf16 tile (Q, K or V)
@@ -359,13 +359,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             } else {
                 const int sl = next_stage(sv);
                 if (sl == sv + 1) {
-                    // Ph [Vh | Vl]: V lo is the next stage, one 64-column block on
+                    // Ph [Vh | Vl] and Pl [Vh | Vl]: V lo is the next stage, one 64-column block
+                    // on, so both are N = 2D products (Pl Vl, about 2^-18 of P V, comes for free)
                     pv_x3(dst, pa, vd, C::IDESC_PV2, acc);
+                    pv_x3(dst, pa + 16, vd, C::IDESC_PV2, true);
                 } else {
                     pv_x3(dst, pa, vd, C::IDESC_PV, acc);
                     pv_x3(dst + D, pa, sdesc_sw128(sRing + sl * C::TILE, C::DBLK, 1024), C::IDESC_PV, acc);
+                    pv_x3(dst, pa + 16, vd, C::IDESC_PV, true);   // + Pl Vh into the first D columns
                 }
-                pv_x3(dst, pa + 16, vd, C::IDESC_PV, true);   // + Pl Vh into the first D columns
             }
         };
         // PV for Q tile t at key tile i of an item; pc[t] counts P handshakes, oe[t] the O
