@@ -96,12 +96,12 @@ SM_COUNT_GB300 = 152
 # each workload's dominant kernel, keyed by the sha256 of the CUDA source it was taken on; a
 # source that changed since the capture reports null.
 TRAFFIC = {
-    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
-                           "bytes": 136.66e6, "scope": "attn_tc_kernel<128>, one launch"},
-    "gqa_causal_prefill_bshd": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
-                                "bytes": 134.10e6, "scope": "attn_tc_kernel<128> on [B, S, H, D] views, one launch"},
-    "gqa_chunked_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
-                            "bytes": 52.07e6, "scope": "attn_tc_kernel<128>, bottom-right mask, one launch"},
+    "gqa_causal_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "33729601088ac731",
+                           "bytes": 136.62e6, "scope": "attn_tc_kernel<128>, one launch"},
+    "gqa_causal_prefill_bshd": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "33729601088ac731",
+                                "bytes": 133.67e6, "scope": "attn_tc_kernel<128> on [B, S, H, D] views, one launch"},
+    "gqa_chunked_prefill": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "33729601088ac731",
+                            "bytes": 52.13e6, "scope": "attn_tc_kernel<128>, bottom-right mask, one launch"},
     "gqa_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "08ba6f0fc6b184f5",
                    "bytes": 1079.13e6, "scope": "decode_kernel<128>, one launch"},
     "gqa_speculative_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "08ba6f0fc6b184f5",
@@ -116,9 +116,9 @@ TRAFFIC = {
                             "bytes": 343.07e6, "scope": "softmax_ex_pair_kernel<bf16, bf16, 64>, one launch"},
     "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "217705f65f3906d7",
                             "bytes": 523.54e6, "scope": "bwd_tc_kernel<128> (dK/dV and dQ CTAs), one launch"},
-    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
+    "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "33729601088ac731",
                              "bytes": 4.34e6, "scope": "attn_tc_kernel<64, x3>, one launch"},
-    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "4ba5f0a9882f85ef",
+    "single_head_4096_bf16": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "33729601088ac731",
                               "bytes": 1.63e6, "scope": "attn_tc_kernel<64>, one launch (8 key splits)"},
 }
 
