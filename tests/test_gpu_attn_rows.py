@@ -73,3 +73,19 @@ def test_solve_is_deterministic(osf):
     osf.osf_attn_fwd(Q, K, V, b, 64, 100, 32)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_scores_and_scale_override(osf, causal):
+    """Scores of a few hundred (Q scaled by 30) and an explicit scale: the running maximum keeps
+    every exponent <= 0 and the per-block rescale stays exact in float32."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 150, 32
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=77 + causal)
+    q = (q * 30.0).astype(np.float32)
+    scale = 0.3
+    lse = torch.empty(B, Hq, S, device="cuda")
+    o = osf.osf_attn_fwd_gqa(f32_tensor(q), f32_tensor(k), f32_tensor(v), causal=causal, scale=scale, lse=lse)
+    ref, ref_lse = oracle.attention_gqa(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
+                                        causal=causal, scale=scale)
+    assert_f32_close(o.cpu().numpy(), ref, atol=1e-4, what=f"large scores causal={causal}")
+    assert_f32_close(lse.cpu().numpy(), ref_lse, atol=1e-3, what="lse")
