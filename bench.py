@@ -106,10 +106,10 @@ TRAFFIC = {
                    "bytes": 1079.13e6, "scope": "decode_kernel<128>, one launch"},
     "gqa_speculative_decode": {"source": "online_softmax_flash_gb300/csrc/decode.cu", "sha": "08ba6f0fc6b184f5",
                                "bytes": 1085.72e6, "scope": "decode_kernel<128>, 16 rows per kv head, one launch"},
-    "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
-                     "bytes": 1012.50e6, "scope": "softmax_rows_resident_kernel<8>, one launch"},
-    "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "ccbf8f037ebe87b8",
-                   "bytes": 756.78e6, "scope": "step: chunk state + chunk normalise kernels"},
+    "softmax_rows": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "aa0692536436b66b",
+                     "bytes": 1013.79e6, "scope": "softmax_rows_resident_kernel<8>, one launch"},
+    "softmax_1d": {"source": "online_softmax_flash_gb300/csrc/softmax.cu", "sha": "aa0692536436b66b",
+                   "bytes": 753.31e6, "scope": "step: chunk state + chunk normalise kernels"},
     "softmax_rows_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "d07ea9a9b6620ae0",
                           "bytes": 475.47e6, "scope": "softmax_ex_split_kernel<bf16, bf16, 256, 8>, one launch"},
     "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "d07ea9a9b6620ae0",

@@ -198,7 +198,24 @@ __device__ __forceinline__ void range_norm(const float *xr, float *zr, long long
         const float4 *x4 = reinterpret_cast<const float4 *>(xr + c0);
         float4 *z4 = reinterpret_cast<float4 *>(zr + c0);
         const long long n4 = (c1 - c0) >> 2;
-        for (long long i = n4 - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
+        // four loads in flight per thread, then their four results
+        const long long step = (long long)blockDim.x;
+        long long i = n4 - 1 - threadIdx.x;
+        for (; i - 3 * step >= 0; i -= 4 * step) {
+            float4 a[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] = x4[i - u * step];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float4 o;
+                o.x = ex2_approx(a[u].x * kLog2e - mref) * inv;
+                o.y = ex2_approx(a[u].y * kLog2e - mref) * inv;
+                o.z = ex2_approx(a[u].z * kLog2e - mref) * inv;
+                o.w = ex2_approx(a[u].w * kLog2e - mref) * inv;
+                __stcs(z4 + i - u * step, o);
+            }
+        }
+        for (; i >= 0; i -= step) {
             const float4 a = x4[i];
             float4 o;
             o.x = ex2_approx(a.x * kLog2e - mref) * inv;
