@@ -89,3 +89,27 @@ def test_backward_rejects_overlaps_and_missing_workspace(osf):
     assert lib.osf_attn_bwd_gqa(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(),
                                 lse.data_ptr(), *(t.data_ptr() for t in out), osf.OSF_BF16, 1, 2, 2, 8, 8, 64, 0,
                                 0.0, None, 0, None) == osf.OSF_ERR_WORKSPACE
+
+
+def test_backward_full_size(osf):
+    """The benchmark's backward (B=2, Hq=32, Hkv=8, S=4096, D=128, causal) in its own launch
+    configuration, every element against the oracle, one kv group at a time (a group's dQ, dK and
+    dV depend only on its own Q, K, V and dO)."""
+    B, Hq, Hkv, S, D = 2, 32, 8, 4096, 128
+    G = Hq // Hkv
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=5, dtype="bf16")
+    g = si.qkv((B, Hq, S, D), (1, 1, 1, D), seed=1005, dtype="bf16")[0]
+    Q, K, V, GO = (bf16_tensor(a) for a in (q, k, v, g))
+    lse = torch.empty(B, Hq, S, device="cuda")
+    O = osf.osf_attn_fwd_gqa_ex(Q, K, V, mask="top_left", lse=lse)
+    dq, dk, dv = osf.osf_attn_bwd_gqa(Q, K, V, O, GO, lse, mask="top_left")
+    torch.cuda.synchronize()
+    for b, kvh in ((b, h) for b in range(B) for h in range(Hkv)):
+        hs = slice(kvh * G, (kvh + 1) * G)
+        rq, rk, rv = oracle.attention_gqa_bwd(f64(q[b:b + 1, hs], "bf16"), f64(k[b:b + 1, kvh:kvh + 1], "bf16"),
+                                              f64(v[b:b + 1, kvh:kvh + 1], "bf16"), f64(g[b:b + 1, hs], "bf16"),
+                                              mask="top_left")
+        what = f"full size b={b} kv head {kvh}"
+        check_grad(dq[b:b + 1, hs], rq, "bf16", what + " dq")
+        check_grad(dk[b:b + 1, kvh:kvh + 1], rk, "bf16", what + " dk")
+        check_grad(dv[b:b + 1, kvh:kvh + 1], rv, "bf16", what + " dv")
