@@ -129,3 +129,15 @@ def test_speculative_rows_on_the_decode_kernel(osf, Sq, mask):
     """G * Sq <= 16 query rows per kv head (here G = 4): the decode kernel with per-row limits."""
     run(osf, 2, 16, 4, Sq, 5003, 128, "bf16", mask, layout="bshd", seed=41 + Sq)
     run(osf, 1, 8, 2, Sq, 700, 64, "bf16", mask, seed=43 + Sq)
+
+
+def test_chunked_prefill_full_size(osf):
+    """The chunked-prefill workload at full size (1024 new rows after a 3072-key cache: B=2,
+    Hq=32, Hkv=8, Sq=1024, Sk=4096, D=128, bottom-right), every element of O and lse."""
+    run(osf, 2, 32, 8, 1024, 4096, 128, "bf16", "bottom_right", seed=53)
+
+
+def test_speculative_decode_full_size(osf):
+    """The speculative-decode workload at full size (4 draft rows per head against a 32768-key
+    cache: B=8, Hq=32, Hkv=8, Sq=4, Sk=32768, D=128, bottom-right), every element of O and lse."""
+    run(osf, 8, 32, 8, 4, 32768, 128, "bf16", "bottom_right", seed=59)
