@@ -109,14 +109,19 @@ int osf_attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, int d
  * Q, O, dO, dQ: [B, Hq, Sq, D]; K, V, dK, dV: [B, Hkv, Sk, D]; all of `dtype`, contiguous,
  * device.  lse: float32 [B, Hq, Sq], the natural-log log-sum-exp the forward call returned.
  * mask, scale: as given to the forward call (an osf_mask; scale <= 0 selects D^-0.5).
- * workspace: osf_attn_bwd_workspace_bytes bytes (one float per query row).
+ * workspace: osf_attn_bwd_workspace_bytes bytes: one float per query row (the row sums D), then,
+ * for bf16 with D in {64, 128} while it stays within 16 GiB, room for dS^T in bf16
+ * (B * Hq * ceil(Sk/128)*128 * ceil(Sq/128)*128 elements).  A workspace of at least the first
+ * part (256-byte rounded) but short of the whole selects the path that keeps no dS.
  * dQ, dK, dV must not overlap one another or any input -> else OSF_ERR_INVALID.
  * B, Sq or Sk == 0: OSF_OK, nothing written.  Other errors as in osf_attn_fwd_gqa.
  * Kernel choice: bf16 with D in {64, 128} whose tensors TMA can address (16-byte aligned
- * pointers) runs a row-sum pre-pass and then one grid of tcgen05 tensor-core CTAs (dK/dV CTAs
- * per key tile, dQ CTAs per query tile; accumulators in TMEM, tiles streamed by TMA); other
- * bf16 D in {64, 128} cases the warp-level mma.sync kernels; everything else a CUDA-core kernel
- * with one warp per row.
+ * pointers) runs a row-sum pre-pass and then tcgen05 tensor-core kernels (accumulators in TMEM,
+ * tiles streamed by TMA): with the full workspace, dK/dV CTAs per key tile that also store dS^T,
+ * then dQ = scale * dS K as one product over the stored dS (three launches); with the shorter
+ * workspace, one grid of dK/dV CTAs and dQ CTAs that recompute S and dP (two launches).  Other
+ * bf16 D in {64, 128} cases run the warp-level mma.sync kernels; everything else a CUDA-core
+ * kernel with one warp per row.
  */
 int osf_attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                      const float *lse, void *dQ, void *dK, void *dV, int dtype, int B, int Hq, int Hkv,

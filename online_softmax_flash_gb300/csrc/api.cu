@@ -625,6 +625,17 @@ int osf_softmax_rows(const float *x, float *z, long long rows, long long T, void
                                              dev->sm_count, (cudaStream_t)stream));
 }
 
+// Bytes of bf16 dS^T the tensor-core backward keeps for its separate dQ product
+// ([B * Hq][Sk rounded up to 128][Sq rounded up to 128]); 0 where that path does not apply or the
+// buffer would pass 16 GiB (dQ then recomputes S and dP instead).
+static size_t bwd_ds_bytes(int dtype, int B, int Hq, int Sq, int Sk, int D) {
+    if (dtype != OSF_BF16 || (D != 64 && D != 128) || B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0) return 0;
+    const size_t cap = (size_t)16 << 30;
+    const size_t tile = ((size_t)Sk + 127) / 128 * 128 * (((size_t)Sq + 127) / 128 * 128) * 2;
+    if (tile > cap / ((size_t)B * (size_t)Hq)) return 0;
+    return align256(tile * (size_t)B * (size_t)Hq);
+}
+
 int osf_attn_bwd_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int D, size_t *bytes) {
     if (!bytes) return OSF_ERR_INVALID;
     *bytes = 0;
@@ -634,7 +645,7 @@ int osf_attn_bwd_workspace_bytes(int dtype, int B, int Hq, int Hkv, int Sq, int 
     int st = check_gqa_ex(ph, ph, ph, reinterpret_cast<void *>(uintptr_t(1) << 44), dtype, B, Hq, Hkv, Sq, Sk, D,
                           nullptr, OSF_MASK_NONE, 0.f, nullptr, p, empty);
     if (st != OSF_OK || empty) return st;
-    *bytes = align256((size_t)B * Hq * Sq * sizeof(float));
+    *bytes = align256((size_t)B * Hq * Sq * sizeof(float)) + bwd_ds_bytes(dtype, B, Hq, Sq, Sk, D);
     return OSF_OK;
 }
 
@@ -678,6 +689,14 @@ int osf_attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O,
     b.scale_log2 = p.scale_log2;
     b.scale = p.scale_log2 / kLog2e;
     b.dvec = static_cast<float *>(workspace);
+    // a workspace that also holds dS^T selects the tensor-core path's separate dQ product
+    const size_t ds_bytes = bwd_ds_bytes(dtype, B, Hq, Sq, Sk, D);
+    if (ds_bytes > 0 && workspace_bytes >= need + ds_bytes &&
+        ((reinterpret_cast<uintptr_t>(workspace) + need) & 31u) == 0) {
+        b.ds = static_cast<char *>(workspace) + need;
+        b.ds_rows = ((long long)Sk + 127) / 128 * 128;
+        b.ds_ld = ((long long)Sq + 127) / 128 * 128;
+    }
     b.status = dev->status;
     return launch_status(launch_attn_bwd(b, (cudaStream_t)stream));
 }

@@ -58,7 +58,9 @@ struct BtCfg {
     static constexpr uint32_t A_OFF = 0;                        // two resident tiles (Q, dO) or (K, V)
     static constexpr uint32_t RING_OFF = 2 * TILE;
     static constexpr uint32_t TAB_OFF = RING_OFF + RING * TILE;  // [TSTAGES][2][128] floats
-    static constexpr uint32_t SMEM_BYTES = TAB_OFF + TSTAGES * 2 * TB * 4 + 1024;
+    // dK/dV with a dS workspace: a 2 KB staging tile per compute warp for the TMA stores of dS^T
+    static constexpr uint32_t STG_OFF = TAB_OFF + TSTAGES * 2 * TB * 4;
+    static constexpr uint32_t SMEM_BYTES = STG_OFF + NCW * 2048 + 1024;
     static constexpr uint32_t IDESC_SS = idesc_bf16_f32(TB, TB, 0, 0);   // [128 x 128] scores
     static constexpr uint32_t IDESC_TS = idesc_bf16_f32(TB, D, 0, 1);    // [128 x D] += P [128 x 128] X
 };
@@ -102,12 +104,16 @@ __device__ __forceinline__ void issue_ss(uint32_t dst, uint32_t a_tile, uint32_t
     }
 }
 
-__device__ __forceinline__ void pack_store16(uint32_t taddr, const float (&v)[32]) {
-    uint32_t pk[16];
+// 32 floats as bf16 pairs `pk` into 16 TMEM columns.
+__device__ __forceinline__ void pack_store16(uint32_t taddr, const float (&v)[32], uint32_t (&pk)[16]) {
 #pragma unroll
     for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
     tmem_st16(taddr, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7], pk[8], pk[9], pk[10], pk[11], pk[12],
               pk[13], pk[14], pk[15]);
+}
+__device__ __forceinline__ void pack_store16(uint32_t taddr, const float (&v)[32]) {
+    uint32_t pk[16];
+    pack_store16(taddr, v, pk);
 }
 
 // 32 columns of TMEM (fp32) times `sc`, as bf16, to global memory when `store`.
@@ -358,7 +364,8 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &mq, const CUtenso
 // ====================================================================== dK, dV
 template <int D>
 __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUtensorMap &mg, const CUtensorMap &mk,
-                                              const CUtensorMap &mv, const BwdProblem &p, unsigned bid) {
+                                              const CUtensorMap &mv, const CUtensorMap &mdst, const BwdProblem &p,
+                                              unsigned bid) {
     using C = BtCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BtBars bars;
@@ -529,7 +536,9 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars.pa));
-            // phase B: dS^T = P^T (dP^T - D_q), bf16 into TMEM
+            // phase B: dS^T = P^T (dP^T - D_q), bf16 into TMEM (and to the workspace when dQ runs
+            // as a separate product)
+            uint32_t dpk[2][16];   // this key's 64 values of dS^T as bf16 pairs
             ok = mbar_wait(smem_u32(&bars.dp_full), j & 1, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -552,7 +561,7 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
                                   ds[k], ds[k + 1]);
                     }
                 }
-                pack_store16(tP + lane_off + col0 + 16 * c, ds);
+                pack_store16(tP + lane_off + col0 + 16 * c, ds, dpk[c]);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -561,8 +570,30 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
                 mbar_arrive(smem_u32(&bars.pb));
                 mbar_arrive(smem_u32(&bars.t_empty[st]));
             }
+            // The workspace copy of dS^T leaves after the hand-off: this warp's [32 keys x 64
+            // queries] through its 2 KB staging tile ([32 rows][64 B], 64-byte swizzle) as two TMA
+            // stores of [32 x 32], so the copy engine, not the load/store unit, writes the rows.
+            if (p.ds) {
+                const uint32_t stg = sbase + C::STG_OFF + (uint32_t)(warp - 4) * 2048u;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    if (lane == 0) bulk_wait_read();   // the previous store has read the tile
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(stg + (uint32_t)lane * 64 + ((uint32_t)(k ^ ((lane >> 1) & 3)) << 4), dpk[c][4 * k],
+                                     dpk[c][4 * k + 1], dpk[c][4 * k + 2], dpk[c][4 * k + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&mdst, stg, qbase + col0 + 32 * c, key0 + q4 * 32, b * p.Hq + hq);
+                        bulk_commit();
+                    }
+                }
+            }
         }
         if (!ok) bt_timeout(&abort_flag, p.status);
+        if (p.ds && lane == 0) bulk_wait_all();   // the dS^T stores have landed
         // epilogue: dK = scale * dS^T Q (warps of half 0), dV = P^T dO (half 1); zero when no
         // query sees this key
         bool have = false;
@@ -594,10 +625,213 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
 template <int D>
 __global__ void __launch_bounds__(NT_THREADS, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mg,
-              const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const BwdProblem p,
-              unsigned n_dkdv) {
-    if (blockIdx.x < n_dkdv) bwd_dkdv_body<D>(mq, mg, mk, mv, p, blockIdx.x);
+              const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+              const __grid_constant__ CUtensorMap mdst, const BwdProblem p, unsigned n_dkdv) {
+    if (blockIdx.x < n_dkdv) bwd_dkdv_body<D>(mq, mg, mk, mv, mdst, p, blockIdx.x);
     else bwd_dq_body<D>(mq, mg, mk, mv, p, blockIdx.x - n_dkdv);
+}
+
+// ====================================================================== dQ as one product
+// With a dS workspace the dK/dV CTAs also store dS^T (bf16 [b, q head][key][query], both counts
+// padded to 128), and dQ = scale * dS K becomes a plain product over the key tiles a query tile
+// sees: S and dP are not recomputed, so a (query tile, key tile) pair costs five products in all
+// instead of seven.  An item is one query tile of `hp` query heads of one kv group (two when the
+// group size is even, so each K tile feeds two heads' products); persistent CTAs (one per SM)
+// walk the items heaviest first, in snake order.  Warp 0 streams the dS^T tiles and warp 6 the K
+// tiles by TMA, each through its own ring (a load takes a couple of microseconds under load, so
+// several of each must be in flight per SM).  Warp 1 issues the MMAs into one of two sets of
+// TMEM accumulators, and warps 2-5 scale and store one set while the next item's products run.
+// Both operands are MN-major in shared memory: a dS^T tile is [128 keys][128 queries] (queries
+// contiguous, two 64-column blocks) and serves as dS, and a K tile is [128 keys][D].
+template <int D>
+struct DqCfg {
+    static constexpr uint32_t A_TILE = TB * TB * 2;
+    static constexpr uint32_t B_TILE = TB * D * 2;
+    static constexpr int K_STAGES = 3;
+    static constexpr int FIT = (int)((232448u - 1024u - K_STAGES * B_TILE) / A_TILE);
+    static constexpr int DS_STAGES = FIT < 6 ? FIT : 6;          // 4 at D = 128, 5 at D = 64
+    static constexpr uint32_t K_OFF = DS_STAGES * A_TILE;
+    static constexpr uint32_t SMEM_BYTES = K_OFF + K_STAGES * B_TILE + 1024;
+    static constexpr uint32_t DBLK = TB * 128;                  // bytes between 64-column blocks
+    static constexpr uint32_t IDESC = idesc_bf16_f32(TB, D, 1, 1);
+    static constexpr uint32_t TMEM_COLS = 4 * D;                // 2 sets x up to 2 heads
+    static_assert(DS_STAGES >= 2 && DS_STAGES <= 6 && K_STAGES <= 4, "ring barriers");
+};
+constexpr int DQ_THREADS = 224;   // warp 0 dS^T loads, 1 MMA, 2-5 epilogue, 6 K loads
+
+struct DqBars {
+    uint64_t ds_full[6], ds_empty[6], k_full[4], k_empty[4], acc_full[2], acc_empty[2], drain;
+};
+
+// Item `it`, heaviest first: its first query row, first (b, q head) index and key-tile count.
+__device__ __forceinline__ void dq_item(const BwdProblem &p, int hp, int it, int &q0, int &bh, int &n) {
+    const int BHP = p.B * p.Hq / hp, nqt = (p.Sq + TB - 1) / TB;
+    q0 = (nqt - 1 - it / BHP) * TB;
+    bh = (it % BHP) * hp;
+    n = (p.Sk + TB - 1) / TB;
+    if (p.causal) {
+        const int last = min(q0 + TB - 1, p.Sq - 1) + p.causal_off;
+        n = min(n, last < 0 ? 0 : last / TB + 1);
+    }
+}
+// This CTA's item of round r (forward on even rounds, backward on odd ones), or -1.
+__device__ __forceinline__ int dq_item_of(int r, int n_items) {
+    const int g = (int)gridDim.x, c = (r & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const long long it = (long long)r * g + c;
+    return it < n_items ? (int)it : -1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CUtensorMap mk, const BwdProblem p,
+                   int hp, int n_items) {
+    using C = DqCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ DqBars bars;
+    __shared__ uint32_t tmem_sh;
+    __shared__ volatile int abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u, sK = sbase + C::K_OFF;
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_sh), C::TMEM_COLS);
+    if (tid == 32) {
+        for (int s = 0; s < C::DS_STAGES; ++s) {
+            mbar_init(smem_u32(&bars.ds_full[s]), 1);
+            mbar_init(smem_u32(&bars.ds_empty[s]), 1);
+        }
+        for (int s = 0; s < C::K_STAGES; ++s) {
+            mbar_init(smem_u32(&bars.k_full[s]), 1);
+            mbar_init(smem_u32(&bars.k_empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars.acc_full[i]), 1);
+            mbar_init(smem_u32(&bars.acc_empty[i]), 4);   // one arrival per epilogue warp
+        }
+        mbar_init(smem_u32(&bars.drain), 1);
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if ((warp == 0 || warp == 6) && lane == 0) {
+        // ------------------------------------------------------------ TMA: dS^T (warp 0), K (warp 6)
+        const bool is_ds = warp == 0;
+        const int stages = is_ds ? C::DS_STAGES : C::K_STAGES, per = is_ds ? hp : 1;
+        const uint32_t tile = is_ds ? C::A_TILE : C::B_TILE, ring = is_ds ? sbase : sK;
+        uint64_t *full = is_ds ? bars.ds_full : bars.k_full, *empty = is_ds ? bars.ds_empty : bars.k_empty;
+        tma_prefetch_desc(is_ds ? &mds : &mk);
+        if (is_ds) griddep_wait();   // dS^T is written by the dK/dV grid this kernel depends on
+        const int G = p.Hq / p.Hkv;
+        bool ok = true;
+        int g = 0;   // tiles streamed so far
+        for (int r = 0; ok; ++r) {
+            const int it = dq_item_of(r, n_items);
+            if (it < 0) break;
+            int q0, bh, n;
+            dq_item(p, hp, it, q0, bh, n);
+            const int b = bh / p.Hq, kvh = (bh % p.Hq) / G;
+            for (int j = 0; j < n && ok; ++j) {
+                for (int h = 0; h < per; ++h, ++g) {
+                    const int st = g % stages;
+                    ok = mbar_wait(smem_u32(&empty[st]), ((g / stages) & 1) ^ 1, &abort_flag);
+                    if (!ok) break;
+                    const uint32_t dst = ring + st * tile;
+                    mbar_expect_tx(smem_u32(&full[st]), tile);
+                    if (is_ds) tma_load_4d(dst, &mds, smem_u32(&full[st]), 0, j * TB, q0 / 64, bh + h);
+                    else tma_load_5d(dst, &mk, smem_u32(&full[st]), 0, j * TB, 0, kvh, b);
+                }
+            }
+        }
+        if (!ok) {
+            bt_timeout(&abort_flag, p.status);
+            bt_settle();
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issue
+        bool ok = true;
+        int gd = 0, gk = 0, a = 0;   // dS^T and K tiles consumed, accumulator sets filled
+        for (int r = 0; ok; ++r) {
+            const int it = dq_item_of(r, n_items);
+            if (it < 0) break;
+            int q0, bh, n;
+            dq_item(p, hp, it, q0, bh, n);
+            if (n == 0) continue;
+            const int buf = a & 1;
+            // the epilogue has read this set's previous item
+            if (a >= 2 && !(ok = mbar_wait_spin(smem_u32(&bars.acc_empty[buf]), ((a >> 1) - 1) & 1, &abort_flag)))
+                break;
+            for (int j = 0; j < n && ok; ++j, ++gk) {
+                const int sk = gk % C::K_STAGES;
+                ok = mbar_wait_spin(smem_u32(&bars.k_full[sk]), (gk / C::K_STAGES) & 1, &abort_flag);
+                const uint64_t bd = sdesc_sw128(sK + sk * C::B_TILE, C::DBLK, 1024);
+                for (int h = 0; h < hp && ok; ++h, ++gd) {
+                    const int sd = gd % C::DS_STAGES;
+                    ok = mbar_wait_spin(smem_u32(&bars.ds_full[sd]), (gd / C::DS_STAGES) & 1, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(sbase + sd * C::A_TILE, C::DBLK, 1024);
+                    const uint32_t dst = tmem + (uint32_t)((buf * 2 + h) * D);
+#pragma unroll
+                    for (int k = 0; k < TB / 16; ++k)   // 16 keys per k-step: 16 rows of both tiles
+                        mma_ss(dst, ad + ((k * 2048) >> 4), bd + ((k * 2048) >> 4), C::IDESC, j > 0 || k > 0);
+                    mma_commit(smem_u32(&bars.ds_empty[sd]));
+                }
+                if (ok) mma_commit(smem_u32(&bars.k_empty[sk]));
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&bars.acc_full[buf]));
+            ++a;
+        }
+        if (!ok) bt_timeout(&abort_flag, p.status);
+        mma_commit(smem_u32(&bars.drain));
+        mbar_wait(smem_u32(&bars.drain), 0, nullptr, 20000000ull);
+    } else if (warp >= 2 && warp <= 5) {
+        // ------------------------------------------------------------ epilogue: dQ = scale * acc
+        const int q4 = warp & 3;   // warps 2-5 cover the four TMEM lane quarters
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        bool ok = true;
+        int a = 0;
+        for (int r = 0;; ++r) {
+            const int it = dq_item_of(r, n_items);
+            if (it < 0) break;
+            int q0, bh, n;
+            dq_item(p, hp, it, q0, bh, n);
+            const int row = q0 + q4 * 32 + lane;
+            const bool row_ok = row < p.Sq;
+            const int buf = a & 1;
+            bool have = false;   // rows that see no key get dQ = 0
+            if (n > 0 && ok) {
+                have = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.acc_full[buf]), (a >> 1) & 1, &abort_flag));
+                if (!have) {
+                    ok = false;
+                    bt_timeout(&abort_flag, p.status);
+                }
+                tc_fence_after();
+            }
+            for (int h = 0; h < hp; ++h) {
+                __nv_bfloat16 *dq =
+                    static_cast<__nv_bfloat16 *>(p.dq) + ((long long)(bh + h) * p.Sq + (row_ok ? row : 0)) * D;
+                const uint32_t src = tmem + (uint32_t)((buf * 2 + h) * D) + lane_off;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_to_bf16(src + c * 32, have, p.scale, row_ok, dq + c * 32);
+            }
+            if (n > 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[buf]));
+                ++a;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
 }
 
 template <int D>
@@ -615,10 +849,33 @@ cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
     const unsigned nkv = (unsigned)((p.Sk + TB - 1) / TB) * (unsigned)(p.B * p.Hkv);
     const unsigned nq = (unsigned)((p.Sq + TB - 1) / TB) * (unsigned)(p.B * p.Hq);
     if ((unsigned long long)nkv + nq >= (1ull << 31)) return cudaErrorInvalidValue;
-    cudaError_t e = launch_dependent(bwd_tc_kernel<D>, dim3(nkv + nq), dim3(NT_THREADS), C::SMEM_BYTES, s, mq, mg, mk,
-                                     mv, p, nkv);
+    if (!p.ds) {
+        // dK/dV and dQ CTAs in one grid
+        cudaError_t e = launch_dependent(bwd_tc_kernel<D>, dim3(nkv + nq), dim3(NT_THREADS), C::SMEM_BYTES, s, mq, mg,
+                                         mk, mv, mq, p, nkv);   // (no dS stores: the fifth map is unused)
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    // dK/dV CTAs (they also store dS^T), then dQ = scale * dS K as a dependent grid
+    using Q = DqCfg<D>;
+    CUtensorMap mds, mdst;
+    if (!make_bf16_tile_map(&mds, p.ds, (int)p.ds_ld, p.ds_rows, (long long)p.B * p.Hq, TB, 2) ||
+        !make_bf16_store_map_32x32(&mdst, p.ds, p.ds_ld, p.ds_rows, (long long)p.B * p.Hq))
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_max_dynamic_smem((const void *)bwd_dq_gemm_kernel<D>, (int)Q::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    count_launches(1);
+    int sms = 0;
+    if (device_sm_count(&sms) != OSF_OK || sms <= 0) return cudaErrorInvalidValue;
+    e = launch_dependent(bwd_tc_kernel<D>, dim3(nkv), dim3(NT_THREADS), C::SMEM_BYTES, s, mq, mg, mk, mv, mdst, p,
+                         nkv);
+    if (e != cudaSuccess) return e;
+    const int hp = (p.Hq / p.Hkv) % 2 == 0 ? 2 : 1;   // query heads per item: two of one kv group
+    const int n_items = (int)nq / hp;
+    e = launch_dependent(bwd_dq_gemm_kernel<D>, dim3((unsigned)min(sms, n_items)), dim3(DQ_THREADS), Q::SMEM_BYTES, s,
+                         mds, mk, p, hp, n_items);
+    if (e != cudaSuccess) return e;
+    count_launches(2);
     return cudaGetLastError();
 }
 

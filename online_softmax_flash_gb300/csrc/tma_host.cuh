@@ -39,6 +39,20 @@ inline bool make_bf16_map_3d(CUtensorMap *m, const void *g, int D, long long Y, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a contiguous bf16 tensor [Z][Y][X] for stores of [32 x 32] boxes (64-byte rows,
+// 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r / 2) % 4) in shared memory).
+inline bool make_bf16_store_map_32x32(CUtensorMap *m, const void *g, long long X, long long Y, long long Z) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)X, (cuuint64_t)Y, (cuuint64_t)Z};
+    cuuint64_t strides[2] = {(cuuint64_t)X * 2, (cuuint64_t)X * 2 * (cuuint64_t)Y};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(g), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D view (d % 64, y, d / 64, z) of a contiguous bf16 tensor [Z][Y][D], D a multiple of 64:
 // one box {64, box_rows, D/64, 1} brings a whole [box_rows x D] tile in a single TMA
 // instruction, laid out in shared memory as D/64 consecutive [box_rows][64] blocks (128-byte

@@ -39,26 +39,36 @@ def check_grad(got, ref, dtype, what):
     assert np.isfinite(g).all(), what + " not finite"
 
 
-def run(osf, B, Hq, Hkv, Sq, Sk, D, dtype, mask, seed=0):
+def rowsum_only_workspace(B, Hq, Sq):
+    """A workspace with room for the row sums alone: the tensor-core path then recomputes S and
+    dP for dQ instead of storing dS."""
+    return torch.empty((B * Hq * Sq * 4 + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
+
+
+def run(osf, B, Hq, Hkv, Sq, Sk, D, dtype, mask, seed=0, store_ds=True):
     q, k, v = si.qkv((B, Hq, Sq, D), (B, Hkv, Sk, D), seed=seed, dtype=dtype)
     g = si.qkv((B, Hq, Sq, D), (1, 1, 1, D), seed=seed + 1000, dtype=dtype)[0]
     dev = bf16_tensor if dtype == "bf16" else f32_tensor
     Q, K, V, G = dev(q), dev(k), dev(v), dev(g)
     lse = torch.empty(B, Hq, Sq, device="cuda")
     O = osf.osf_attn_fwd_gqa_ex(Q, K, V, mask=mask, lse=lse)
-    dq, dk, dv = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask=mask)
+    ws = None if store_ds else rowsum_only_workspace(B, Hq, Sq)
+    dq, dk, dv = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask=mask, workspace=ws)
     rq, rk, rv = oracle.attention_gqa_bwd(f64(q, dtype), f64(k, dtype), f64(v, dtype), f64(g, dtype), mask=mask)
-    what = f"{dtype} {B},{Hq},{Hkv},{Sq},{Sk},{D} {mask}"
+    what = f"{dtype} {B},{Hq},{Hkv},{Sq},{Sk},{D} {mask} store_ds={store_ds}"
     check_grad(dq, rq, dtype, what + " dq")
     check_grad(dk, rk, dtype, what + " dk")
     check_grad(dv, rv, dtype, what + " dv")
 
 
+@pytest.mark.parametrize("store_ds", [True, False])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("mask", ["none", "top_left", "bottom_right"])
-def test_bf16_tensor_core_backward(osf, D, mask):
+def test_bf16_tensor_core_backward(osf, D, mask, store_ds):
+    """Both tensor-core paths: dS stored and dQ as one product over it (the default workspace),
+    and dQ recomputing S and dP (a workspace of row sums only)."""
     Sk = 333 if mask == "bottom_right" else 200
-    run(osf, 1, 4, 2, 200, Sk, D, "bf16", mask, seed=D)
+    run(osf, 1, 4, 2, 200, Sk, D, "bf16", mask, seed=D, store_ds=store_ds)
 
 
 @pytest.mark.parametrize("mask", ["none", "top_left", "bottom_right"])
@@ -71,11 +81,40 @@ def test_bf16_other_head_dims_backward(osf, D):
     run(osf, 2, 4, 4, 77, 77, D, "bf16", "top_left", seed=D)
 
 
-def test_backward_ragged_multi_block_gqa(osf):
-    """Several key and query blocks with ragged ends, G = 4, bottom-right with Sq > Sk
-    (rows without keys must send back nothing)."""
-    run(osf, 2, 8, 2, 300, 190, 128, "bf16", "bottom_right", seed=11)
-    run(osf, 1, 8, 2, 1000, 1000, 64, "bf16", "top_left", seed=12)
+@pytest.mark.parametrize("store_ds", [True, False])
+def test_backward_ragged_multi_block_gqa(osf, store_ds):
+    """Several key and query blocks with ragged ends, G = 4 and G = 3 (the dQ product pairs the
+    query heads of a group when G is even), bottom-right with Sq > Sk (rows without keys must send
+    back nothing), and more query tiles than SMs hold items at once."""
+    run(osf, 2, 8, 2, 300, 190, 128, "bf16", "bottom_right", seed=11, store_ds=store_ds)
+    run(osf, 1, 8, 2, 1000, 1000, 64, "bf16", "top_left", seed=12, store_ds=store_ds)
+    run(osf, 3, 16, 4, 1100, 700, 128, "bf16", "none", seed=13, store_ds=store_ds)
+    run(osf, 1, 6, 2, 260, 300, 64, "bf16", "top_left", seed=14, store_ds=store_ds)   # odd group size
+
+
+def test_backward_paths_agree_and_repeat(osf):
+    """The stored-dS path and the recomputing path give the same dK and dV bit for bit (the dK/dV
+    CTAs are the same; storing dS only adds writes) and dQ within bf16 rounding of each other; each
+    path repeats its own result exactly."""
+    B, Hq, Hkv, S, D = 1, 8, 2, 700, 128
+    q, k, v = si.qkv((B, Hq, S, D), (B, Hkv, S, D), seed=21, dtype="bf16")
+    g = si.qkv((B, Hq, S, D), (1, 1, 1, D), seed=1021, dtype="bf16")[0]
+    Q, K, V, G = (bf16_tensor(a) for a in (q, k, v, g))
+    lse = torch.empty(B, Hq, S, device="cuda")
+    O = osf.osf_attn_fwd_gqa_ex(Q, K, V, mask="top_left", lse=lse)
+    a = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask="top_left")
+    a2 = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask="top_left")
+    small = rowsum_only_workspace(B, Hq, S)
+    r = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask="top_left", workspace=small)
+    r2 = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask="top_left", workspace=small)
+    torch.cuda.synchronize()
+    for x, y in zip(a, a2):
+        assert torch.equal(x, y)
+    for x, y in zip(r, r2):
+        assert torch.equal(x, y)
+    assert torch.equal(a[1], r[1]) and torch.equal(a[2], r[2])
+    d = (a[0].float() - r[0].float()).abs().max().item()
+    assert d <= 2e-2 * r[0].float().abs().max().item(), d
 
 
 def test_backward_rejects_overlaps_and_missing_workspace(osf):
