@@ -625,9 +625,9 @@ int osf_softmax_rows(const float *x, float *z, long long rows, long long T, void
                                              dev->sm_count, (cudaStream_t)stream));
 }
 
-// Bytes of bf16 dS^T the tensor-core backward keeps for its separate dQ product
-// ([B * Hq][Sk rounded up to 128][Sq rounded up to 128]); 0 where that path does not apply or the
-// buffer would pass 16 GiB (dQ then recomputes S and dP instead).
+// Bytes of bf16 dS^T the tensor-core backward keeps for its separate dQ product ([128 x 128]
+// tiles covering [B * Hq][Sk rounded up to 128][Sq rounded up to 128]); 0 where that path does not
+// apply or the buffer would pass 16 GiB (dQ then recomputes S and dP instead).
 static size_t bwd_ds_bytes(int dtype, int B, int Hq, int Sq, int Sk, int D) {
     if (dtype != OSF_BF16 || (D != 64 && D != 128) || B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0) return 0;
     const size_t cap = (size_t)16 << 30;

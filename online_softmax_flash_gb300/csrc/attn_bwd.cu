@@ -85,6 +85,41 @@ __global__ void __launch_bounds__(256) bwd_rowdot_vec_kernel(BwdProblem p) {
     }
 }
 
+// bf16 with D = 8 * LPR and 16-byte aligned rows: LPR lanes per row, one 16-byte load of O and
+// of dO per lane and row, four rounds of 32 / LPR rows per warp, every load issued before any
+// arithmetic; the partial sums meet within each group of LPR lanes.
+template <int LPR>
+__global__ void __launch_bounds__(256) bwd_rowdot_v16_kernel(BwdProblem p) {
+    constexpr int RPI = 32 / LPR, IT = 4, RPW = RPI * IT;
+    const long long rows = (long long)p.B * p.Hq * p.Sq;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
+    const long long wrow = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
+    uint4 o[IT], g[IT];
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const long long row = wrow + i * RPI + sub;
+        if (row < rows) {
+            o[i] = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.o) + row * p.D)[c];
+            g[i] = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.dout) + row * p.D)[c];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const long long row = wrow + i * RPI + sub;
+        float acc = 0.f;
+        if (row < rows) {
+            const uint32_t ow[4] = {o[i].x, o[i].y, o[i].z, o[i].w}, gw[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                acc += __uint_as_float(ow[w] << 16) * __uint_as_float(gw[w] << 16) +
+                       __uint_as_float(ow[w] & 0xffff0000u) * __uint_as_float(gw[w] & 0xffff0000u);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (c == 0 && row < rows) p.dvec[row] = acc;
+    }
+}
+
 // ------------------------------------------------------------------ CUDA-core version
 // One warp per query row: dQ_i = scale * sum_j dS_ij K_j.
 template <typename T>
@@ -522,7 +557,12 @@ cudaError_t launch_attn_bwd(const BwdProblem &p, cudaStream_t s) {
     const unsigned g = (unsigned)((rows + 7) / 8);
     const bool vec_ok = p.dtype == OSF_BF16 && (p.D == 64 || p.D == 128) &&
                         ((reinterpret_cast<uintptr_t>(p.o) | reinterpret_cast<uintptr_t>(p.dout)) & 7u) == 0;
-    if (vec_ok) {
+    const bool v16_ok = vec_ok && ((reinterpret_cast<uintptr_t>(p.o) | reinterpret_cast<uintptr_t>(p.dout)) & 15u) == 0;
+    if (v16_ok) {
+        // 8 warps x (4 rounds of 32 / LPR rows) per CTA
+        if (p.D == 128) bwd_rowdot_v16_kernel<16><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p);
+        else bwd_rowdot_v16_kernel<8><<<(unsigned)((rows + 127) / 128), 256, 0, s>>>(p);
+    } else if (vec_ok) {
         const unsigned g4 = (unsigned)((rows + 31) / 32);   // 8 warps x 4 rows per CTA
         if (p.D == 128) bwd_rowdot_vec_kernel<4><<<g4, 256, 0, s>>>(p);
         else bwd_rowdot_vec_kernel<2><<<g4, 256, 0, s>>>(p);

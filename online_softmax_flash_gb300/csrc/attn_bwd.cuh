@@ -12,8 +12,10 @@ struct BwdProblem {
     int causal, causal_off;  // key j visible to row i iff !causal || j <= i + causal_off
     float scale, scale_log2;
     float *dvec;           // workspace [B, Hq, Sq]: rowsum(dO * O)
-    // optional workspace (tensor-core path): dS^T as bf16 [B * Hq][ds_rows][ds_ld], ds_rows and
-    // ds_ld the key and query counts rounded up to 128; null: dQ recomputes S and dP instead
+    // optional workspace (tensor-core path): dS^T as bf16 [128 x 128] tiles, tile (bh, key tile,
+    // query tile) at ((bh * ds_rows / 128 + key tile) * ds_ld / 128 + query tile) * 32 KB, each
+    // [128 keys][128 queries]; ds_rows and ds_ld the key and query counts rounded up to 128.
+    // null: dQ recomputes S and dP instead
     void *ds;
     long long ds_rows, ds_ld;
     int *status;

@@ -586,7 +586,9 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&mdst, stg, qbase + col0 + 32 * c, key0 + q4 * 32, b * p.Hq + hq);
+                        const int nkt = (int)(p.ds_rows / TB), nqt = (int)(p.ds_ld / TB);
+                        const int tile = (((b * p.Hq + hq) * nkt) + key0 / TB) * nqt + qbase / TB;
+                        tma_store_3d(&mdst, stg, col0 + 32 * c, q4 * 32, tile);
                         bulk_commit();
                     }
                 }
@@ -632,8 +634,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 }
 
 // ====================================================================== dQ as one product
-// With a dS workspace the dK/dV CTAs also store dS^T (bf16 [b, q head][key][query], both counts
-// padded to 128), and dQ = scale * dS K becomes a plain product over the key tiles a query tile
+// With a dS workspace the dK/dV CTAs also store dS^T (bf16, one contiguous 32 KB [128 keys][128
+// queries] tile per (b, q head, key tile, query tile), so a tile load reads one run of HBM), and dQ = scale * dS K becomes a plain product over the key tiles a query tile
 // sees: S and dP are not recomputed, so a (query tile, key tile) pair costs five products in all
 // instead of seven.  An item is one query tile of `hp` query heads of one kv group (two when the
 // group size is even, so each K tile feeds two heads' products); persistent CTAs (one per SM)
@@ -714,6 +716,9 @@ bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_sh;
+    // dS^T is written by the dK/dV grid this kernel depends on; every role waits for it here, so
+    // no bounded wait below starts counting before that grid has finished
+    griddep_wait();
 
     if ((warp == 0 || warp == 6) && lane == 0) {
         // ------------------------------------------------------------ TMA: dS^T (warp 0), K (warp 6)
@@ -722,7 +727,6 @@ bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constan
         const uint32_t tile = is_ds ? C::A_TILE : C::B_TILE, ring = is_ds ? sbase : sK;
         uint64_t *full = is_ds ? bars.ds_full : bars.k_full, *empty = is_ds ? bars.ds_empty : bars.k_empty;
         tma_prefetch_desc(is_ds ? &mds : &mk);
-        if (is_ds) griddep_wait();   // dS^T is written by the dK/dV grid this kernel depends on
         const int G = p.Hq / p.Hkv;
         bool ok = true;
         int g = 0;   // tiles streamed so far
@@ -739,7 +743,9 @@ bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constan
                     if (!ok) break;
                     const uint32_t dst = ring + st * tile;
                     mbar_expect_tx(smem_u32(&full[st]), tile);
-                    if (is_ds) tma_load_4d(dst, &mds, smem_u32(&full[st]), 0, j * TB, q0 / 64, bh + h);
+                    if (is_ds)
+                        tma_load_4d(dst, &mds, smem_u32(&full[st]), 0, 0, 0,
+                                    (int)(((long long)(bh + h) * (p.ds_rows / TB) + j) * (p.ds_ld / TB) + q0 / TB));
                     else tma_load_5d(dst, &mk, smem_u32(&full[st]), 0, j * TB, 0, kvh, b);
                 }
             }
@@ -860,8 +866,9 @@ cudaError_t launch_t(const BwdProblem &p, cudaStream_t s) {
     // dK/dV CTAs (they also store dS^T), then dQ = scale * dS K as a dependent grid
     using Q = DqCfg<D>;
     CUtensorMap mds, mdst;
-    if (!make_bf16_tile_map(&mds, p.ds, (int)p.ds_ld, p.ds_rows, (long long)p.B * p.Hq, TB, 2) ||
-        !make_bf16_store_map_32x32(&mdst, p.ds, p.ds_ld, p.ds_rows, (long long)p.B * p.Hq))
+    const long long n_tiles = (long long)p.B * p.Hq * (p.ds_rows / TB) * (p.ds_ld / TB);
+    if (!make_bf16_tile_map(&mds, p.ds, TB, TB, n_tiles, TB, 2) ||
+        !make_bf16_store_map_32x32(&mdst, p.ds, TB, TB, n_tiles))
         return cudaErrorInvalidValue;
     cudaError_t e = set_max_dynamic_smem((const void *)bwd_dq_gemm_kernel<D>, (int)Q::SMEM_BYTES);
     if (e != cudaSuccess) return e;
