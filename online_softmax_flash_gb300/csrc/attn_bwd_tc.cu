@@ -411,7 +411,9 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
             int hq, qt;
             step_at(m >> 1, hq, qt);
             mbar_expect_tx(smem_u32(&bars.full[st]), C::TILE);
-            tma_load_5d(sRing + st * C::TILE, (m & 1) ? &mg : &mq, smem_u32(&bars.full[st]), 0, qt * TB, 0, hq, b);
+            // Q and dO tiles are read again by the CTAs of the other key tiles: keep them in L2
+            tma_load_5d_hint(sRing + st * C::TILE, (m & 1) ? &mg : &mq, smem_u32(&bars.full[st]), 0, qt * TB, 0, hq, b,
+                             l2_policy_evict_last());
         }
         if (!ok) {
             bt_timeout(&abort_flag, p.status);
@@ -588,7 +590,8 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
                     if (lane == 0) {
                         const int nkt = (int)(p.ds_rows / TB), nqt = (int)(p.ds_ld / TB);
                         const int tile = (((b * p.Hq + hq) * nkt) + key0 / TB) * nqt + qbase / TB;
-                        tma_store_3d(&mdst, stg, col0 + 32 * c, q4 * 32, tile);
+                        // dS^T is read once, by the dQ product: it gives way in L2 first
+                        tma_store_3d_hint(&mdst, stg, col0 + 32 * c, q4 * 32, tile, l2_policy_evict_first());
                         bulk_commit();
                     }
                 }
@@ -743,9 +746,10 @@ bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constan
                     if (!ok) break;
                     const uint32_t dst = ring + st * tile;
                     mbar_expect_tx(smem_u32(&full[st]), tile);
-                    if (is_ds)
-                        tma_load_4d(dst, &mds, smem_u32(&full[st]), 0, 0, 0,
-                                    (int)(((long long)(bh + h) * (p.ds_rows / TB) + j) * (p.ds_ld / TB) + q0 / TB));
+                    if (is_ds)   // read once: evict first, so the K tiles and dQ rows stay in L2
+                        tma_load_4d_hint(dst, &mds, smem_u32(&full[st]), 0, 0, 0,
+                                         (int)(((long long)(bh + h) * (p.ds_rows / TB) + j) * (p.ds_ld / TB) + q0 / TB),
+                                         l2_policy_evict_first());
                     else tma_load_5d(dst, &mk, smem_u32(&full[st]), 0, j * TB, 0, kvh, b);
                 }
             }
