@@ -114,7 +114,7 @@ TRAFFIC = {
                           "bytes": 475.47e6, "scope": "softmax_ex_split_kernel<bf16, bf16, 256, 8>, one launch"},
     "softmax_causal_bf16": {"source": "online_softmax_flash_gb300/csrc/softmax_ex.cu", "sha": "d07ea9a9b6620ae0",
                             "bytes": 343.07e6, "scope": "softmax_ex_pair_kernel<bf16, bf16, 64>, one launch"},
-    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "4d5b6a783ac0b771",
+    "gqa_causal_backward": {"source": "online_softmax_flash_gb300/csrc/attn_bwd_tc.cu", "sha": "6b2edd0b274b2cfa",
                             "bytes": 1441.99e6,
                             "scope": "bwd_tc_kernel<128> (dK/dV CTAs, writing 1.07 GB of dS^T), one launch"},
     "single_head_4096_f32": {"source": "online_softmax_flash_gb300/csrc/attn_tc.cu", "sha": "33729601088ac731",

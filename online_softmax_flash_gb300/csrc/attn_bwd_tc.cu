@@ -20,9 +20,12 @@
 //   columns, then dV += P^T dO_j;  B: dS^T over dP^T, then dK += dS^T Q_j.
 //   Issuer A: dV_j then S^T_{j+1} (while phase B runs); issuer B: dK_j then dP^T_{j+1} (while
 //   phase A of step j+1 runs).
-// dQ kernel: one CTA per (b, q head, 128 query rows), Q and dO resident, K_j, V_j streamed:
-//   S = Q K_j^T, dP = dO V_j^T;  phase A releases S (issuer A issues S_{j+1} at once);  phase B
-//   writes dS as bf16 into its own columns, then issuer B issues dQ += dS K_j and dP_{j+1}.
+// dQ, two ways.  With a dS workspace (the default) the dK/dV CTAs also store dS^T and a separate
+// persistent product computes dQ = scale * dS K over it (bwd_dq_gemm_kernel, below).  Without
+// one, dQ CTAs run in the dK/dV grid: one CTA per (b, q head, 128 query rows), Q and dO
+// resident, K_j, V_j streamed: S = Q K_j^T, dP = dO V_j^T;  phase A releases S (issuer A issues
+// S_{j+1} at once);  phase B writes dS as bf16 into its own columns, then issuer B issues
+// dQ += dS K_j and dP_{j+1}.
 //
 // TMEM (512 columns).  dK/dV: S^T [0,128), dP^T [128,256), dK [256,256+D), dV [256+D,256+2D).
 // dQ: S [0,128), dP [128,256), dQ [256,256+D), dS (bf16) [256+D,256+D+64).
@@ -638,9 +641,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 
 // ====================================================================== dQ as one product
 // With a dS workspace the dK/dV CTAs also store dS^T (bf16, one contiguous 32 KB [128 keys][128
-// queries] tile per (b, q head, key tile, query tile), so a tile load reads one run of HBM), and dQ = scale * dS K becomes a plain product over the key tiles a query tile
-// sees: S and dP are not recomputed, so a (query tile, key tile) pair costs five products in all
-// instead of seven.  An item is one query tile of `hp` query heads of one kv group (two when the
+// queries] tile per (b, q head, key tile, query tile), so a tile load reads one run of HBM), and
+// dQ = scale * dS K becomes a plain product over the key tiles a query tile sees: S and dP are
+// not recomputed, so a (query tile, key tile) pair costs five products in all instead of seven.  An item is one query tile of `hp` query heads of one kv group (two when the
 // group size is even, so each K tile feeds two heads' products); persistent CTAs (one per SM)
 // walk the items heaviest first, in snake order.  Warp 0 streams the dS^T tiles and warp 6 the K
 // tiles by TMA, each through its own ring (a load takes a couple of microseconds under load, so
