@@ -153,3 +153,29 @@ def test_header_is_plain_c(tmp_path):
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER), str(src)],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_backward_workspace_sizes(osf):
+    """osf_attn_bwd_workspace_bytes: the row sums (one float per query row, 256-byte rounded),
+    plus, for bf16 with D in {64, 128} while it stays within 16 GiB, bf16 dS^T over the key and
+    query counts rounded up to 128; other dtypes, head dims and larger problems get the row sums
+    alone (the path that recomputes S and dP for dQ)."""
+    lib = osf.lib()
+    n = ctypes.c_size_t(0)
+    r256 = lambda x: (x + 255) // 256 * 256
+    r128 = lambda x: (x + 127) // 128 * 128
+
+    def bytes_for(dt, B, Hq, Hkv, Sq, Sk, D):
+        assert lib.osf_attn_bwd_workspace_bytes(dt, B, Hq, Hkv, Sq, Sk, D, ctypes.byref(n)) == osf.OSF_OK
+        return n.value
+
+    for (B, Hq, Hkv, Sq, Sk, D) in [(2, 32, 8, 4096, 4096, 128), (1, 4, 2, 200, 333, 64), (3, 16, 4, 1100, 700, 128)]:
+        rows = r256(B * Hq * Sq * 4)
+        assert bytes_for(osf.OSF_BF16, B, Hq, Hkv, Sq, Sk, D) == rows + r256(B * Hq * r128(Sk) * r128(Sq) * 2)
+        assert bytes_for(osf.OSF_F32, B, Hq, Hkv, Sq, Sk, D if D == 64 else 128) == rows
+    assert bytes_for(osf.OSF_BF16, 1, 4, 2, 77, 77, 96) == r256(4 * 77 * 4)
+    # dS^T past 16 GiB: the row sums alone
+    B, Hq, S = 2, 64, 65536
+    assert B * Hq * S * S * 2 > 16 << 30
+    assert bytes_for(osf.OSF_BF16, B, Hq, 8, S, S, 128) == r256(B * Hq * S * 4)
+    assert bytes_for(osf.OSF_BF16, 1, 1, 1, 0, 8, 128) == 0
