@@ -580,14 +580,19 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &mq, const CUten
             // stores of [32 x 32], so the copy engine, not the load/store unit, writes the rows.
             if (p.ds) {
                 const uint32_t stg = sbase + C::STG_OFF + (uint32_t)(warp - 4) * 2048u;
+                // rows of keys past Sk are zero: their K rows are zero-filled, so P^T there is
+                // 2^-lse, which overflows for rows whose scores are all far below zero, and the
+                // dQ product must not meet inf * 0
+                const uint32_t keep = key < p.Sk ? 0xffffffffu : 0u;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     if (lane == 0) bulk_wait_read();   // the previous store has read the tile
                     __syncwarp();
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        st_shared_v4(stg + (uint32_t)lane * 64 + ((uint32_t)(k ^ ((lane >> 1) & 3)) << 4), dpk[c][4 * k],
-                                     dpk[c][4 * k + 1], dpk[c][4 * k + 2], dpk[c][4 * k + 3]);
+                        st_shared_v4(stg + (uint32_t)lane * 64 + ((uint32_t)(k ^ ((lane >> 1) & 3)) << 4),
+                                     dpk[c][4 * k] & keep, dpk[c][4 * k + 1] & keep, dpk[c][4 * k + 2] & keep,
+                                     dpk[c][4 * k + 3] & keep);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {

@@ -152,3 +152,30 @@ def test_backward_full_size(osf):
         check_grad(dq[b:b + 1, hs], rq, "bf16", what + " dq")
         check_grad(dk[b:b + 1, kvh:kvh + 1], rk, "bf16", what + " dk")
         check_grad(dv[b:b + 1, kvh:kvh + 1], rv, "bf16", what + " dv")
+
+
+@pytest.mark.parametrize("store_ds", [True, False])
+def test_backward_rows_with_very_negative_scores_and_a_ragged_key_tail(osf, store_ds):
+    """Every score of every row far below zero (Q and K pointing apart, scale 10) with Sk not a
+    multiple of 128: lse is near -370, so e^-lse overflows float32 for the zero-filled key rows
+    past Sk, and those rows must not reach dQ.  The gradients stay finite and match the oracle.
+    (The K offset is kept to about the spread of K: with a large common offset the bf16 rounding of
+    dS alone, amplified by |K|, reaches the bf16 bound in dQ whatever the kernel.)"""
+    B, Hq, Hkv, Sq, Sk, D, scale = 1, 4, 2, 150, 190, 64, 10.0
+    k = np.abs(si.normal_f32((B, Hkv, Sk, D), 31, si.STREAM_K)) * np.float32(0.5) + np.float32(0.5)
+    q = -np.abs(si.normal_f32((B, Hq, Sq, D), 31, si.STREAM_Q)) * np.float32(0.5) - np.float32(0.5)
+    v = si.normal_f32((B, Hkv, Sk, D), 31, si.STREAM_V)
+    g = si.normal_f32((B, Hq, Sq, D), 32, si.STREAM_V)
+    qb, kb, vb, gb = (si.f32_to_bf16_bits(a) for a in (q, k, v, g))
+    Q, K, V, G = (bf16_tensor(a) for a in (qb, kb, vb, gb))
+    lse = torch.empty(B, Hq, Sq, device="cuda")
+    O = osf.osf_attn_fwd_gqa_ex(Q, K, V, mask="none", scale=scale, lse=lse)
+    assert float(lse.max()) < -100.0   # e^100 is past the float32 range
+    ws = None if store_ds else rowsum_only_workspace(B, Hq, Sq)
+    dq, dk, dv = osf.osf_attn_bwd_gqa(Q, K, V, O, G, lse, mask="none", scale=scale, workspace=ws)
+    rq, rk, rv = oracle.attention_gqa_bwd(f64(qb, "bf16"), f64(kb, "bf16"), f64(vb, "bf16"), f64(gb, "bf16"),
+                                          mask="none", scale=scale)
+    what = f"very negative scores store_ds={store_ds}"
+    check_grad(dq, rq, "bf16", what + " dq")
+    check_grad(dk, rk, "bf16", what + " dk")
+    check_grad(dv, rv, "bf16", what + " dv")
